@@ -1,0 +1,158 @@
+"""Thin ctypes binding of libhsa.so (include/hsa.h).
+
+Argument marshalling only: every step runs in the library's CUDA kernels.
+Functions keep the C names; tensors are torch CUDA tensors (device memory and
+streams come from torch), sizes and strides are taken from them.  There is no
+CPU path: if the shared library is missing or fails to load, importing this
+module raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libhsa.so")
+
+HSA_OK, HSA_ERR_INVALID_ARG, HSA_ERR_UNSUPPORTED, HSA_ERR_WORKSPACE, HSA_ERR_CUDA, HSA_ERR_DEVICE_FLAG = range(6)
+HSA_F32, HSA_BF16 = 0, 1
+_STATUS = {0: "HSA_OK", 1: "HSA_ERR_INVALID_ARG", 2: "HSA_ERR_UNSUPPORTED", 3: "HSA_ERR_WORKSPACE",
+           4: "HSA_ERR_CUDA", 5: "HSA_ERR_DEVICE_FLAG"}
+
+# every symbol include/hsa.h declares
+EXPORTS = ["hsa_last_error", "hsa_version", "hsa_check", "hsa_compress", "hsa_index_topk_workspace_size",
+           "hsa_index_topk", "hsa_attn_decode_workspace_size", "hsa_attn_decode",
+           "hsa_attn_prefill_workspace_size", "hsa_attn_prefill"]
+
+
+class HSAError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"{_STATUS.get(status, status)}: {msg}")
+        self.status = status
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is missing: build it with `python -m compressed_attention_compress_b300.build`")
+    lib = ctypes.CDLL(LIB_PATH)
+    P, I, I64, SZ, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float
+    lib.hsa_last_error.restype = ctypes.c_char_p
+    lib.hsa_last_error.argtypes = []
+    lib.hsa_version.restype = I
+    lib.hsa_check.restype = I
+    lib.hsa_check.argtypes = [P]
+    lib.hsa_compress.restype = I
+    lib.hsa_compress.argtypes = [P, P, I, I, I, I64, I64, I64, P, P, I64, P, I, P, P, I64, I64, I64, P]
+    lib.hsa_index_topk_workspace_size.restype = I
+    lib.hsa_index_topk_workspace_size.argtypes = [I, I, I, I64, I, ctypes.POINTER(SZ)]
+    lib.hsa_index_topk.restype = I
+    lib.hsa_index_topk.argtypes = [P, I64, I64, P, I64, I64, I64, I, I, I, P, I, I, P, P, P, SZ, P]
+    lib.hsa_attn_decode_workspace_size.restype = I
+    lib.hsa_attn_decode_workspace_size.argtypes = [I, I, I, I, I64, I, I, I, ctypes.POINTER(SZ)]
+    lib.hsa_attn_decode.restype = I
+    lib.hsa_attn_decode.argtypes = [P, I, I, I, I, P, P, I64, I64, I64, I, P, P, I, P, P, I64, I64, I64, I, P, F,
+                                    P, P, P, SZ, P]
+    lib.hsa_attn_prefill_workspace_size.restype = I
+    lib.hsa_attn_prefill_workspace_size.argtypes = [I, I, I, I, I, I64, I, I, I, ctypes.POINTER(SZ)]
+    lib.hsa_attn_prefill.restype = I
+    lib.hsa_attn_prefill.argtypes = [P, I, I, I, I, I, P, P, I64, I64, I64, I, P, P, I, P, P, I64, I64, I64, I, P,
+                                     F, P, P, P, SZ, P]
+    return lib
+
+
+lib = _load()
+
+
+def _chk(status: int):
+    if status != HSA_OK:
+        raise HSAError(status, lib.hsa_last_error().decode())
+
+
+def _p(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _dt(t):
+    if t.dtype == torch.bfloat16:
+        return HSA_BF16
+    if t.dtype == torch.float32:
+        return HSA_F32
+    raise HSAError(HSA_ERR_UNSUPPORTED, f"dtype {t.dtype}")
+
+
+def hsa_check(stream=None):
+    _chk(lib.hsa_check(_stream(stream)))
+
+
+def hsa_compress(k, v, tok_begin, tok_end, max_blocks, w, m, kc, vc, stream=None):
+    """k, v [B, N_cap, d]; kc, vc [B, E_cap, d] (channel stride 1); tok_* int64 [B] on device."""
+    B, N_cap, d = k.shape
+    assert v.shape == k.shape and v.stride() == k.stride() and kc.stride() == vc.stride()
+    _chk(lib.hsa_compress(_p(k), _p(v), _dt(k), B, d, k.stride(0), k.stride(1), N_cap, _p(tok_begin), _p(tok_end),
+                          int(max_blocks), _p(w), int(m), _p(kc), _p(vc), kc.stride(0), kc.stride(1), kc.shape[1],
+                          _stream(stream)))
+
+
+def hsa_index_topk_workspace_size(B, T, DI, E_cap, topk):
+    n = ctypes.c_size_t(0)
+    _chk(lib.hsa_index_topk_workspace_size(B, T, DI, E_cap, topk, ctypes.byref(n)))
+    return n.value
+
+
+def hsa_index_topk(q_idx, k_idx, q_pos0, m, topk, idx_out, cnt_out, ws, stream=None):
+    """q_idx int8 [B, T, DI]; k_idx int8 [B, E_cap, DI]; idx_out int32 [B, T, topk]; cnt_out int32 [B, T]."""
+    B, T, DI = q_idx.shape
+    E_cap = k_idx.shape[1]
+    _chk(lib.hsa_index_topk(_p(q_idx), q_idx.stride(0), q_idx.stride(1), _p(k_idx), k_idx.stride(0), k_idx.stride(1),
+                            E_cap, B, T, DI, _p(q_pos0), int(m), int(topk), _p(idx_out), _p(cnt_out), _p(ws),
+                            ws.numel() * ws.element_size() if ws is not None else 0, _stream(stream)))
+
+
+def hsa_attn_decode_workspace_size(dtype, B, H, d, E_cap, m, topk, window):
+    n = ctypes.c_size_t(0)
+    dt = HSA_BF16 if dtype == torch.bfloat16 else HSA_F32
+    _chk(lib.hsa_attn_decode_workspace_size(dt, B, H, d, E_cap, m, topk, window, ctypes.byref(n)))
+    return n.value
+
+
+def hsa_attn_decode(q, kc, vc, m, idx, cnt, k_raw, v_raw, window, ctx_len, scale, out, lse=None, ws=None,
+                    stream=None):
+    """q [B, H, d]; kc/vc [B, E_cap, d]; idx int32 [B, topk] or None (HCA); out [B, H, d]; lse fp32 [B, H]."""
+    B, H, d = q.shape
+    topk = idx.shape[-1] if idx is not None else 0
+    _chk(lib.hsa_attn_decode(_p(q), _dt(q), B, H, d, _p(kc), _p(vc), kc.stride(0), kc.stride(1), kc.shape[1],
+                             int(m), _p(idx), _p(cnt), topk, _p(k_raw), _p(v_raw), k_raw.stride(0), k_raw.stride(1),
+                             k_raw.shape[1], int(window), _p(ctx_len), float(scale), _p(out), _p(lse), _p(ws),
+                             ws.numel() * ws.element_size() if ws is not None else 0, _stream(stream)))
+
+
+def hsa_attn_prefill_workspace_size(dtype, B, T, H, d, E_cap, m, topk, window):
+    n = ctypes.c_size_t(0)
+    dt = HSA_BF16 if dtype == torch.bfloat16 else HSA_F32
+    _chk(lib.hsa_attn_prefill_workspace_size(dt, B, T, H, d, E_cap, m, topk, window, ctypes.byref(n)))
+    return n.value
+
+
+def hsa_attn_prefill(q, kc, vc, m, idx, cnt, k_raw, v_raw, window, q_pos0, scale, out, lse=None, ws=None,
+                     stream=None):
+    """q [B, T, H, d]; idx int32 [B, T, topk] or None (HCA); out [B, T, H, d]; lse fp32 [B, T, H]."""
+    B, T, H, d = q.shape
+    topk = idx.shape[-1] if idx is not None else 0
+    _chk(lib.hsa_attn_prefill(_p(q), _dt(q), B, T, H, d, _p(kc), _p(vc), kc.stride(0), kc.stride(1), kc.shape[1],
+                              int(m), _p(idx), _p(cnt), topk, _p(k_raw), _p(v_raw), k_raw.stride(0),
+                              k_raw.stride(1), k_raw.shape[1], int(window), _p(q_pos0), float(scale), _p(out),
+                              _p(lse), _p(ws), ws.numel() * ws.element_size() if ws is not None else 0,
+                              _stream(stream)))
+
+
+def workspace(nbytes: int, device="cuda"):
+    """A zero-filled, 256-byte aligned workspace (torch allocations are 512-byte aligned)."""
+    return torch.zeros(max(int(nbytes), 1), dtype=torch.uint8, device=device)

@@ -1,0 +1,67 @@
+// Shared device helpers of the CUDA path (sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace hsa {
+
+// Sticky device-side range-violation flag (one per device, per loaded module).
+// Kernels OR a bit in and skip the offending access; hsa_check() reads it.
+extern __device__ unsigned int g_device_flag;  // defined in hsa_api.cu (relocatable device code)
+
+enum : unsigned {
+    FLAG_COMPRESS_RANGE = 1u << 0,
+    FLAG_INDEX_RANGE = 1u << 1,
+    FLAG_ATTN_RANGE = 1u << 2,
+    FLAG_ATTN_INDEX = 1u << 3,
+};
+
+__device__ __forceinline__ void raise_flag(unsigned bit) { atomicOr(&g_device_flag, bit); }
+
+__device__ __forceinline__ int64_t num_entries(int64_t p, int m) { return p < 0 ? 0 : (p + 1) / m; }
+
+template <typename T>
+struct ElemTraits;
+template <>
+struct ElemTraits<float> {
+    static constexpr int kVec = 4;  // elements per 16 bytes
+};
+template <>
+struct ElemTraits<__nv_bfloat16> {
+    static constexpr int kVec = 8;
+};
+
+__device__ __forceinline__ float bf16_lo(uint32_t u) { return __uint_as_float(u << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);  // RNE, lo in the low half
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// 16-byte async copy global -> shared; src_bytes = 0 zero-fills the destination.
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src, int src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(src_bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ int4 ld_nc_v4(const void *p) {
+    int4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.s32 {%0,%1,%2,%3}, [%4];\n"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+
+}  // namespace hsa

@@ -1,0 +1,118 @@
+// KV compression: every m consecutive K (and V) tokens fold into one entry,
+// C[b, j, :] = sum_{r<m} w[r] * X[b, j*m + r, :]   (QbitAI article "DeepSeek V4报告太详尽了！",
+// section 混合注意力机制: CSA step 1 and the HCA paragraph, m' = 128 with no overlap).
+//
+// HBM-bound: every input byte is read once with 16-byte vector loads, rows are
+// coalesced (consecutive threads own consecutive 16-byte channel chunks of the
+// same token), the weighted sum is accumulated in fp32 in the order r = 0..m-1
+// and rounded once to the storage type.  K and V are handled by the same launch
+// (blockIdx.y selects the tensor).
+#include "common.cuh"
+#include "internal.h"
+
+namespace hsa {
+
+template <typename T, int U>
+__global__ void __launch_bounds__(256) compress_kernel(CompressArgs a) {
+    constexpr int V = ElemTraits<T>::kVec;
+    extern __shared__ float s_w[];
+    for (int r = threadIdx.x; r < a.m; r += blockDim.x) s_w[r] = a.w[r];
+    __syncthreads();
+
+    const T *__restrict__ x = static_cast<const T *>(blockIdx.y == 0 ? a.k : a.v);
+    T *__restrict__ out = static_cast<T *>(blockIdx.y == 0 ? a.kc : a.vc);
+    const int nvec = a.d / V;
+    const int64_t per_b = a.max_blocks * nvec;
+    const int64_t total = per_b * a.B;
+    for (int64_t item = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; item < total;
+         item += (int64_t)gridDim.x * blockDim.x) {
+        const int b = (int)(item / per_b);
+        const int64_t rem = item - b * per_b;
+        const int64_t jl = rem / nvec;
+        const int c = (int)(rem - jl * nvec);
+        const int64_t j0 = a.tok_begin[b] / a.m, j1 = a.tok_end[b] / a.m;
+        const int64_t j = j0 + jl;
+        if (j >= j1) continue;
+        if (a.tok_begin[b] < 0 || (j + 1) * a.m > a.N_cap || j >= a.E_cap) {
+            raise_flag(FLAG_COMPRESS_RANGE);
+            continue;
+        }
+        const char *src = reinterpret_cast<const char *>(x + b * a.in_sb + j * a.m * a.in_st + c * V);
+        const int64_t step = a.in_st * (int64_t)sizeof(T);
+        float acc[V];
+#pragma unroll
+        for (int e = 0; e < V; ++e) acc[e] = 0.f;
+        int r = 0;
+        for (; r + U <= a.m; r += U) {
+            int4 buf[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) buf[u] = ld_nc_v4(src + (r + u) * step);
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const float wr = s_w[r + u];
+                const uint32_t *p = reinterpret_cast<const uint32_t *>(&buf[u]);
+                if constexpr (V == 8) {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        acc[2 * e] = fmaf(wr, bf16_lo(p[e]), acc[2 * e]);
+                        acc[2 * e + 1] = fmaf(wr, bf16_hi(p[e]), acc[2 * e + 1]);
+                    }
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) acc[e] = fmaf(wr, __uint_as_float(p[e]), acc[e]);
+                }
+            }
+        }
+        for (; r < a.m; ++r) {
+            const int4 bv = ld_nc_v4(src + r * step);
+            const float wr = s_w[r];
+            const uint32_t *p = reinterpret_cast<const uint32_t *>(&bv);
+            if constexpr (V == 8) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    acc[2 * e] = fmaf(wr, bf16_lo(p[e]), acc[2 * e]);
+                    acc[2 * e + 1] = fmaf(wr, bf16_hi(p[e]), acc[2 * e + 1]);
+                }
+            } else {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) acc[e] = fmaf(wr, __uint_as_float(p[e]), acc[e]);
+            }
+        }
+        int4 o;
+        uint32_t *op = reinterpret_cast<uint32_t *>(&o);
+        if constexpr (V == 8) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) op[e] = pack_bf16x2(acc[2 * e], acc[2 * e + 1]);
+        } else {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) op[e] = __float_as_uint(acc[e]);
+        }
+        *reinterpret_cast<int4 *>(out + b * a.out_sb + j * a.out_se + c * V) = o;
+    }
+}
+
+cudaError_t launch_compress(const CompressArgs &a, bool bf16, int num_sms, cudaStream_t s) {
+    const int V = bf16 ? 8 : 4;
+    const int64_t total = a.max_blocks * (a.d / V) * a.B;
+    if (total <= 0) return cudaSuccess;
+    const int threads = 256;
+    int64_t want = (total + threads - 1) / threads;
+    const int64_t cap = (int64_t)num_sms * 8;
+    const int grid_x = (int)(want < cap ? want : cap);
+    const size_t smem = sizeof(float) * a.m;
+    dim3 grid(grid_x, 2);
+    if (bf16) {
+        if (a.m >= 8)
+            compress_kernel<__nv_bfloat16, 8><<<grid, threads, smem, s>>>(a);
+        else
+            compress_kernel<__nv_bfloat16, 4><<<grid, threads, smem, s>>>(a);
+    } else {
+        if (a.m >= 8)
+            compress_kernel<float, 8><<<grid, threads, smem, s>>>(a);
+        else
+            compress_kernel<float, 4><<<grid, threads, smem, s>>>(a);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace hsa

@@ -1,0 +1,324 @@
+// C-ABI layer: argument validation, workspace carving and launch sequencing.
+// Every entry point enqueues on the caller's stream and never allocates,
+// frees or synchronises (hsa_check excepted).
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include "../../include/hsa.h"
+#include "common.cuh"
+#include "internal.h"
+
+namespace hsa {
+__device__ unsigned int g_device_flag = 0;
+}
+
+namespace {
+
+thread_local char t_err[512] = "";
+
+hsa_status_t fail(hsa_status_t st, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(t_err, sizeof t_err, fmt, ap);
+    va_end(ap);
+    return st;
+}
+
+hsa_status_t ok() {
+    t_err[0] = '\0';
+    return HSA_OK;
+}
+
+struct DevInfo {
+    int num_sms = 0;
+    int major = 0, minor = 0;
+};
+
+hsa_status_t device_info(DevInfo &di) {
+    static thread_local int cached_dev = -1;
+    static thread_local DevInfo cached;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail(HSA_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+    if (dev != cached_dev) {
+        cudaDeviceProp pr;
+        e = cudaGetDeviceProperties(&pr, dev);
+        if (e != cudaSuccess) return fail(HSA_ERR_CUDA, "cudaGetDeviceProperties: %s", cudaGetErrorString(e));
+        cached.num_sms = pr.multiProcessorCount;
+        cached.major = pr.major;
+        cached.minor = pr.minor;
+        cached_dev = dev;
+    }
+    di = cached;
+    if (di.major != 10) return fail(HSA_ERR_UNSUPPORTED, "device sm_%d%d: this library is built for sm_103a", di.major, di.minor);
+    return HSA_OK;
+}
+
+hsa_status_t pending_error() {
+    cudaError_t e = cudaPeekAtLastError();
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(HSA_ERR_CUDA, "pending CUDA error: %s", cudaGetErrorString(e));
+    }
+    return HSA_OK;
+}
+
+hsa_status_t launched(cudaError_t e, const char *what) {
+    if (e != cudaSuccess) return fail(HSA_ERR_CUDA, "%s launch: %s", what, cudaGetErrorString(e));
+    return ok();
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+size_t esize(hsa_dtype_t dt) { return dt == HSA_BF16 ? 2 : 4; }
+bool dtype_ok(hsa_dtype_t dt) { return dt == HSA_BF16 || dt == HSA_F32; }
+
+// Rows of the indexer handled per launch group: bounded so that the stored keys
+// stay under 1 GiB of workspace.
+int index_group_rows(int rows, int64_t E_cap) {
+    const int64_t per_row = (E_cap > 0 ? E_cap : 1) * 4 + 65536;
+    int64_t g = (1ll << 30) / per_row;
+    if (g < 1) g = 1;
+    return (int)(g < rows ? g : rows);
+}
+
+// Decode attention split planning: the split size depends on the shape only, and
+// the split count of a row on its own set size.
+struct DecodePlan {
+    int split, max_splits;
+    size_t off_o, off_lse, total;
+};
+DecodePlan plan_decode(hsa_dtype_t dt, int B, int H, int d, int64_t E_cap, int m, int topk, int window,
+                       bool dense, int num_sms) {
+    DecodePlan p{};
+    (void)m;
+    const int64_t max_items = (dense ? E_cap : (int64_t)topk) + window;
+    p.split = hsa::attn_split_size(dt == HSA_BF16, dense, H, B, max_items, num_sms);
+    if (p.split <= 0) {
+        p.max_splits = 1;
+        p.total = 0;
+        return p;
+    }
+    p.max_splits = (int)((max_items + p.split - 1) / p.split);
+    if (p.max_splits < 1) p.max_splits = 1;
+    p.off_o = 0;
+    p.off_lse = ((size_t)B * p.max_splits * H * d * sizeof(float) + 255) & ~(size_t)255;
+    p.total = p.off_lse + (((size_t)B * p.max_splits * H * sizeof(float) + 255) & ~(size_t)255);
+    return p;
+}
+
+hsa_status_t check_attn_common(const void *q, hsa_dtype_t dt, int B, int T, int H, int d, const void *kc,
+                               const void *vc, int64_t c_sb, int64_t c_se, int64_t E_cap, int m,
+                               const int32_t *idx, int topk, const void *k_raw, const void *v_raw, int64_t r_sb,
+                               int64_t r_st, int64_t N_cap, int window, const int64_t *pos, const void *out) {
+    if (!dtype_ok(dt)) return fail(HSA_ERR_UNSUPPORTED, "dtype %d", (int)dt);
+    if (B < 0 || T < 0 || H <= 0 || d <= 0 || m <= 0 || window < 0 || E_cap < 0 || N_cap < 0)
+        return fail(HSA_ERR_INVALID_ARG, "negative or zero size (B=%d T=%d H=%d d=%d m=%d window=%d)", B, T, H, d, m,
+                    window);
+    if (idx && topk <= 0) return fail(HSA_ERR_INVALID_ARG, "topk must be positive when idx is given");
+    if (B * (int64_t)T == 0) return HSA_OK;
+    if (!q || !out || !pos) return fail(HSA_ERR_INVALID_ARG, "null q/out/position pointer");
+    if (window > 0 && (!k_raw || !v_raw)) return fail(HSA_ERR_INVALID_ARG, "null raw cache with window > 0");
+    if (E_cap > 0 && (!kc || !vc)) return fail(HSA_ERR_INVALID_ARG, "null compressed cache");
+    if (dt == HSA_BF16) {
+        if (d != 64 && d != 128) return fail(HSA_ERR_UNSUPPORTED, "bf16 path supports d in {64,128}, got %d", d);
+        if (H % 16 != 0 || H > 128) return fail(HSA_ERR_UNSUPPORTED, "bf16 path needs H a multiple of 16 up to 128, got %d", H);
+    } else {
+        if (d % 32 != 0 || d > 256) return fail(HSA_ERR_UNSUPPORTED, "fp32 path needs d a multiple of 32 up to 256, got %d", d);
+    }
+    const size_t es = esize(dt);
+    const int64_t vec = 16 / (int64_t)es;
+    if (!aligned16(q) || !aligned16(out) || (kc && !aligned16(kc)) || (vc && !aligned16(vc)) ||
+        (k_raw && !aligned16(k_raw)) || (v_raw && !aligned16(v_raw)))
+        return fail(HSA_ERR_UNSUPPORTED, "q, out and caches must be 16-byte aligned");
+    if (c_sb % vec || c_se % vec || r_sb % vec || r_st % vec)
+        return fail(HSA_ERR_UNSUPPORTED, "cache strides must be multiples of 16 bytes");
+    if (c_se < d || r_st < d || c_sb < 0 || r_sb < 0) return fail(HSA_ERR_INVALID_ARG, "cache strides overlap rows");
+    return HSA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *hsa_last_error(void) { return t_err; }
+
+int hsa_version(void) { return 100; }
+
+hsa_status_t hsa_check(hsa_stream_t stream) {
+    cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail(HSA_ERR_CUDA, "stream: %s", cudaGetErrorString(e));
+    unsigned flag = 0;
+    e = cudaMemcpyFromSymbol(&flag, hsa::g_device_flag, sizeof flag);
+    if (e != cudaSuccess) return fail(HSA_ERR_CUDA, "reading device flag: %s", cudaGetErrorString(e));
+    if (flag) {
+        const unsigned zero = 0;
+        e = cudaMemcpyToSymbol(hsa::g_device_flag, &zero, sizeof zero);
+        if (e != cudaSuccess) return fail(HSA_ERR_CUDA, "clearing device flag: %s", cudaGetErrorString(e));
+        return fail(HSA_ERR_DEVICE_FLAG, "device range flag 0x%x (1=compress 2=index 4=attn range 8=attn index)", flag);
+    }
+    return ok();
+}
+
+hsa_status_t hsa_compress(const void *k, const void *v, hsa_dtype_t dt, int B, int d, int64_t in_sb, int64_t in_st,
+                          int64_t N_cap, const int64_t *tok_begin, const int64_t *tok_end, int64_t max_blocks,
+                          const float *w, int m, void *kc, void *vc, int64_t out_sb, int64_t out_se, int64_t E_cap,
+                          hsa_stream_t stream) {
+    if (!dtype_ok(dt)) return fail(HSA_ERR_UNSUPPORTED, "dtype %d", (int)dt);
+    if (B < 0 || d <= 0 || m <= 0 || max_blocks < 0 || N_cap < 0 || E_cap < 0)
+        return fail(HSA_ERR_INVALID_ARG, "bad size (B=%d d=%d m=%d max_blocks=%lld)", B, d, m, (long long)max_blocks);
+    if (m > 4096) return fail(HSA_ERR_UNSUPPORTED, "m > 4096");
+    if (B == 0 || max_blocks == 0) return ok();
+    if (!k || !v || !kc || !vc || !tok_begin || !tok_end || !w) return fail(HSA_ERR_INVALID_ARG, "null pointer");
+    const int64_t vec = 16 / (int64_t)esize(dt);
+    if (d % vec || d > 512) return fail(HSA_ERR_UNSUPPORTED, "d must be a multiple of %lld and <= 512", (long long)vec);
+    if (!aligned16(k) || !aligned16(v) || !aligned16(kc) || !aligned16(vc))
+        return fail(HSA_ERR_UNSUPPORTED, "tensors must be 16-byte aligned");
+    if (in_sb % vec || in_st % vec || out_sb % vec || out_se % vec)
+        return fail(HSA_ERR_UNSUPPORTED, "strides must be multiples of 16 bytes");
+    if (in_st < d || out_se < d) return fail(HSA_ERR_INVALID_ARG, "row strides overlap rows");
+    DevInfo di;
+    hsa_status_t st = device_info(di);
+    if (st != HSA_OK) return st;
+    if ((st = pending_error()) != HSA_OK) return st;
+    hsa::CompressArgs a{k, v, B, d, in_sb, in_st, N_cap, tok_begin, tok_end, max_blocks, w, m, kc, vc, out_sb, out_se, E_cap};
+    return launched(hsa::launch_compress(a, dt == HSA_BF16, di.num_sms, reinterpret_cast<cudaStream_t>(stream)),
+                    "compress");
+}
+
+hsa_status_t hsa_index_topk_workspace_size(int B, int T, int DI, int64_t E_cap, int topk, size_t *bytes) {
+    if (!bytes) return fail(HSA_ERR_INVALID_ARG, "null bytes");
+    if (B < 0 || T < 0 || E_cap < 0 || topk <= 0 || DI <= 0) return fail(HSA_ERR_INVALID_ARG, "bad size");
+    DevInfo di;
+    hsa_status_t st = device_info(di);
+    if (st != HSA_OK) return st;
+    const int rows = B * T;
+    if (rows == 0) {
+        *bytes = 0;
+        return ok();
+    }
+    const hsa::IndexPlan p = hsa::plan_index(index_group_rows(rows, E_cap), DI, E_cap, topk, di.num_sms);
+    *bytes = p.total;
+    return ok();
+}
+
+hsa_status_t hsa_index_topk(const int8_t *q_idx, int64_t q_sb, int64_t q_st, const int8_t *k_idx, int64_t k_sb,
+                            int64_t k_se, int64_t E_cap, int B, int T, int DI, const int64_t *q_pos0, int m, int topk,
+                            int32_t *idx_out, int32_t *cnt_out, void *ws, size_t ws_bytes, hsa_stream_t stream) {
+    if (B < 0 || T < 0 || E_cap < 0 || m <= 0) return fail(HSA_ERR_INVALID_ARG, "bad size");
+    if (topk <= 0 || topk > 4096) return fail(HSA_ERR_UNSUPPORTED, "topk must be in [1, 4096], got %d", topk);
+    if (DI != 16 && DI != 32 && DI != 64 && DI != 128)
+        return fail(HSA_ERR_UNSUPPORTED, "indexer dim must be 16, 32, 64 or 128, got %d", DI);
+    const int rows = B * T;
+    if (rows == 0) return ok();
+    if (!q_idx || !k_idx || !q_pos0 || !idx_out || !cnt_out) return fail(HSA_ERR_INVALID_ARG, "null pointer");
+    if (E_cap > (int64_t)1 << 30) return fail(HSA_ERR_UNSUPPORTED, "E_cap above 2^30");
+    if (!aligned16(q_idx) || !aligned16(k_idx) || q_sb % 16 || q_st % 16 || k_sb % 16 || k_se % 16)
+        return fail(HSA_ERR_UNSUPPORTED, "indexer tensors and strides must be 16-byte aligned");
+    if (k_se < DI || q_st < DI) return fail(HSA_ERR_INVALID_ARG, "indexer strides overlap rows");
+    DevInfo di;
+    hsa_status_t st = device_info(di);
+    if (st != HSA_OK) return st;
+    const int G = index_group_rows(rows, E_cap);
+    const hsa::IndexPlan p = hsa::plan_index(G, DI, E_cap, topk, di.num_sms);
+    if (!ws || ws_bytes < p.total)
+        return fail(HSA_ERR_WORKSPACE, "index workspace needs %zu bytes, got %zu", p.total, ws_bytes);
+    if ((reinterpret_cast<uintptr_t>(ws) & 255) != 0) return fail(HSA_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+    if ((st = pending_error()) != HSA_OK) return st;
+    hsa::IndexArgs a{q_idx, q_sb, q_st, k_idx, k_sb, k_se, E_cap, B, T, DI, q_pos0, m, topk, idx_out, cnt_out};
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (E_cap == 0) {
+        // no entry can be visible: everything is padding
+        cudaError_t e = cudaMemsetAsync(idx_out, 0xff, sizeof(int32_t) * (size_t)rows * topk, s);
+        if (e == cudaSuccess) e = cudaMemsetAsync(cnt_out, 0, sizeof(int32_t) * (size_t)rows, s);
+        return launched(e, "index (empty)");
+    }
+    for (int r0 = 0; r0 < rows; r0 += G) {
+        cudaError_t e = hsa::launch_index_topk(a, p, ws, r0, s);
+        if (e != cudaSuccess) return launched(e, "index_topk");
+    }
+    return ok();
+}
+
+hsa_status_t hsa_attn_decode_workspace_size(hsa_dtype_t dt, int B, int H, int d, int64_t E_cap, int m, int topk,
+                                            int window, size_t *bytes) {
+    if (!bytes) return fail(HSA_ERR_INVALID_ARG, "null bytes");
+    if (B < 0 || H <= 0 || d <= 0 || E_cap < 0 || window < 0) return fail(HSA_ERR_INVALID_ARG, "bad size");
+    DevInfo di;
+    hsa_status_t st = device_info(di);
+    if (st != HSA_OK) return st;
+    // topk <= 0 means dense (HCA)
+    const DecodePlan p = plan_decode(dt, B, H, d, E_cap, m, topk, window, topk <= 0, di.num_sms);
+    *bytes = p.total;
+    return ok();
+}
+
+hsa_status_t hsa_attn_decode(const void *q, hsa_dtype_t dt, int B, int H, int d, const void *kc, const void *vc,
+                             int64_t c_sb, int64_t c_se, int64_t E_cap, int m, const int32_t *idx, const int32_t *cnt,
+                             int topk, const void *k_raw, const void *v_raw, int64_t r_sb, int64_t r_st,
+                             int64_t N_cap, int window, const int64_t *ctx_len, float scale, void *out, float *lse,
+                             void *ws, size_t ws_bytes, hsa_stream_t stream) {
+    hsa_status_t st = check_attn_common(q, dt, B, 1, H, d, kc, vc, c_sb, c_se, E_cap, m, idx, topk, k_raw, v_raw,
+                                        r_sb, r_st, N_cap, window, ctx_len, out);
+    if (st != HSA_OK) return st;
+    if (B == 0) return ok();
+    DevInfo di;
+    if ((st = device_info(di)) != HSA_OK) return st;
+    const bool dense = idx == nullptr;
+    const DecodePlan p = plan_decode(dt, B, H, d, E_cap, m, dense ? 0 : topk, window, dense, di.num_sms);
+    if (p.total > 0 && (!ws || ws_bytes < p.total))
+        return fail(HSA_ERR_WORKSPACE, "decode workspace needs %zu bytes, got %zu", p.total, ws_bytes);
+    if (p.total > 0 && (reinterpret_cast<uintptr_t>(ws) & 255) != 0)
+        return fail(HSA_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+    if ((st = pending_error()) != HSA_OK) return st;
+    hsa::AttnArgs a{};
+    a.q = q; a.rows = B; a.T = 1; a.H = H; a.d = d;
+    a.kc = kc; a.vc = vc; a.c_sb = c_sb; a.c_se = c_se; a.E_cap = E_cap; a.m = m;
+    a.idx = idx; a.cnt = cnt; a.topk = dense ? 0 : topk;
+    a.k_raw = k_raw; a.v_raw = v_raw; a.r_sb = r_sb; a.r_st = r_st; a.N_cap = N_cap; a.window = window;
+    a.pos = ctx_len; a.pos_is_ctx = 1; a.scale = scale; a.out = out; a.lse = lse;
+    a.split = p.split; a.max_splits = p.max_splits;
+    a.part_o = p.total ? reinterpret_cast<float *>(static_cast<char *>(ws) + p.off_o) : nullptr;
+    a.part_lse = p.total ? reinterpret_cast<float *>(static_cast<char *>(ws) + p.off_lse) : nullptr;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = dt == HSA_BF16 ? hsa::launch_attn_bf16(a, s) : hsa::launch_attn_f32(a, s);
+    if (e != cudaSuccess) return launched(e, "attn_decode");
+    return launched(hsa::launch_attn_merge(a, dt == HSA_BF16, s), "attn_merge");
+}
+
+hsa_status_t hsa_attn_prefill_workspace_size(hsa_dtype_t dt, int B, int T, int H, int d, int64_t E_cap, int m,
+                                             int topk, int window, size_t *bytes) {
+    (void)dt; (void)B; (void)T; (void)H; (void)d; (void)E_cap; (void)m; (void)topk; (void)window;
+    if (!bytes) return fail(HSA_ERR_INVALID_ARG, "null bytes");
+    *bytes = 0;
+    return ok();
+}
+
+hsa_status_t hsa_attn_prefill(const void *q, hsa_dtype_t dt, int B, int T, int H, int d, const void *kc,
+                              const void *vc, int64_t c_sb, int64_t c_se, int64_t E_cap, int m, const int32_t *idx,
+                              const int32_t *cnt, int topk, const void *k_raw, const void *v_raw, int64_t r_sb,
+                              int64_t r_st, int64_t N_cap, int window, const int64_t *q_pos0, float scale, void *out,
+                              float *lse, void *ws, size_t ws_bytes, hsa_stream_t stream) {
+    (void)ws; (void)ws_bytes;
+    hsa_status_t st = check_attn_common(q, dt, B, T, H, d, kc, vc, c_sb, c_se, E_cap, m, idx, topk, k_raw, v_raw,
+                                        r_sb, r_st, N_cap, window, q_pos0, out);
+    if (st != HSA_OK) return st;
+    if (B == 0 || T == 0) return ok();
+    DevInfo di;
+    if ((st = device_info(di)) != HSA_OK) return st;
+    if ((int64_t)B * T > (1ll << 24)) return fail(HSA_ERR_UNSUPPORTED, "B*T above 2^24");
+    if ((st = pending_error()) != HSA_OK) return st;
+    const bool dense = idx == nullptr;
+    hsa::AttnArgs a{};
+    a.q = q; a.rows = B * T; a.T = T; a.H = H; a.d = d;
+    a.kc = kc; a.vc = vc; a.c_sb = c_sb; a.c_se = c_se; a.E_cap = E_cap; a.m = m;
+    a.idx = idx; a.cnt = cnt; a.topk = dense ? 0 : topk;
+    a.k_raw = k_raw; a.v_raw = v_raw; a.r_sb = r_sb; a.r_st = r_st; a.N_cap = N_cap; a.window = window;
+    a.pos = q_pos0; a.pos_is_ctx = 0; a.scale = scale; a.out = out; a.lse = lse;
+    a.split = 0; a.max_splits = 1;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = dt == HSA_BF16 ? hsa::launch_attn_bf16(a, s) : hsa::launch_attn_f32(a, s);
+    return launched(e, "attn_prefill");
+}
+
+}  // extern "C"

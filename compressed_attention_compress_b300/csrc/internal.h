@@ -1,0 +1,79 @@
+// Internal launch interface between the C-ABI layer (hsa_api.cu) and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace hsa {
+
+struct CompressArgs {
+    const void *k, *v;
+    int B, d;
+    int64_t in_sb, in_st, N_cap;
+    const int64_t *tok_begin, *tok_end;
+    int64_t max_blocks;
+    const float *w;
+    int m;
+    void *kc, *vc;
+    int64_t out_sb, out_se, E_cap;
+};
+cudaError_t launch_compress(const CompressArgs &a, bool bf16, int num_sms, cudaStream_t s);
+
+// ---------------------------------------------------------------- indexer
+struct IndexArgs {
+    const int8_t *q;
+    int64_t q_sb, q_st;
+    const int8_t *k;
+    int64_t k_sb, k_se, E_cap;
+    int B, T, DI;
+    const int64_t *q_pos0;
+    int m, topk;
+    int32_t *idx_out, *cnt_out;
+};
+// Workspace layout of the decode-shaped indexer (all offsets 256-byte aligned).
+struct IndexPlan {
+    int rows;          // rows handled by one launch group
+    int chunk;         // entries per CTA
+    int nchunks;       // max chunks per row (grid.x)
+    int key_bits;      // bits of the biased score key
+    int shift1;        // level-1 histogram uses key >> shift1 (256 bins)
+    int cap;           // candidate capacity per row
+    size_t off_keys, off_hist1, off_tick, off_sel, off_runs, off_cand_u, off_cand_j, total;
+};
+IndexPlan plan_index(int rows, int DI, int64_t E_cap, int topk, int num_sms);
+cudaError_t launch_index_topk(const IndexArgs &a, const IndexPlan &p, void *ws, int row_begin,
+                              cudaStream_t s);
+
+// -------------------------------------------------------------- attention
+struct AttnArgs {
+    const void *q;      // [rows, H, d]
+    int rows;           // B * T
+    int T;              // queries per sequence (row r -> b = r / T, t = r % T)
+    int H, d;
+    const void *kc, *vc;
+    int64_t c_sb, c_se, E_cap;
+    int m;
+    const int32_t *idx;  // [rows, topk] or null (dense)
+    const int32_t *cnt;  // [rows] or null
+    int topk;
+    const void *k_raw, *v_raw;
+    int64_t r_sb, r_st, N_cap;
+    int window;
+    const int64_t *pos;  // decode: ctx_len[b] (p = ctx_len - 1); prefill: q_pos0[b] (p = q_pos0 + t)
+    int pos_is_ctx;
+    float scale;
+    void *out;          // [rows, H, d]
+    float *lse;         // [rows, H] or null
+    // split-KV partials (decode)
+    int split;          // items per split; <= 0 -> one split per row
+    int max_splits;
+    float *part_o;      // [rows, max_splits, H, d]
+    float *part_lse;    // [rows, max_splits, H]
+};
+int attn_split_size(bool bf16, bool dense, int H, int rows, int64_t max_items, int num_sms);
+cudaError_t launch_attn_bf16(const AttnArgs &a, cudaStream_t s);
+cudaError_t launch_attn_f32(const AttnArgs &a, cudaStream_t s);
+cudaError_t launch_attn_merge(const AttnArgs &a, bool bf16, cudaStream_t s);
+
+}  // namespace hsa

@@ -1,0 +1,197 @@
+/*
+ * hsa.h -- C ABI of the B300 (sm_103a) hybrid compressed/sparse attention library.
+ *
+ * One attention layer of DeepSeek-V4-style long-context attention, as the
+ * QbitAI article "DeepSeek V4报告太详尽了！484天换代之路全公开" describes it in
+ * its section 混合注意力机制 ("hybrid attention"):
+ *   - CSA: every m tokens' K/V are compressed into one entry, a light indexer
+ *     scores each query against every entry, the top-k entries are attended
+ *     (Multi-Query Attention, one KV head);
+ *   - HCA: heavier compression (m' = 128), dense attention over all entries;
+ *   - both add a sliding-window branch over the most recent raw tokens, and
+ *     compressed attention is strictly causal: only complete blocks count.
+ * The pages leave the compressor and the indexer open; this library fixes
+ * them: an entry is a fixed weighted sum of its block (weights w[0..m-1]), the
+ * indexer score is the int32 dot product of int8 vectors, top-k orders by
+ * (score desc, index asc), and the selected entries and the window share one
+ * softmax with logit scale `scale` (normally 1/sqrt(d)).
+ *
+ * Conventions (all entry points):
+ *   - Every buffer argument is caller-owned DEVICE memory of the current CUDA
+ *     device unless stated otherwise.  The library never allocates, frees or
+ *     synchronises (except hsa_check); all work is enqueued on `stream`
+ *     (a cudaStream_t; NULL is the legacy default stream).
+ *   - Strides are in ELEMENTS.  The innermost (channel) dimension is
+ *     contiguous.  Vector loads need 16-byte aligned base pointers and row
+ *     strides that are multiples of 16 bytes; otherwise HSA_ERR_UNSUPPORTED.
+ *   - Sequence lengths and positions live in device arrays, so a captured CUDA
+ *     graph can be replayed with new lengths.  Host-side size arguments
+ *     (N_cap, E_cap, ...) are buffer CAPACITIES and bound the launch grids.
+ *   - A call returns HSA_OK once its kernels are enqueued.  Argument errors
+ *     return before anything is enqueued and leave the stream untouched.
+ *     Asynchronous CUDA errors surface on the next call or through hsa_check.
+ *     Device-side range violations (a position or index outside its buffer)
+ *     never fault: the offending access is skipped, the output for that item
+ *     is unspecified, and a sticky device flag is raised that hsa_check
+ *     reports as HSA_ERR_DEVICE_FLAG.
+ *   - hsa_last_error() returns a thread-local message for the last failing
+ *     call on this thread.
+ *   - Workspaces are caller-owned device scratch sized by the matching
+ *     *_workspace_size call.  A workspace must be zero-filled once before its
+ *     first use (cudaMemset); every successful call leaves it zero-filled
+ *     again.  Calls that share a workspace must not run concurrently.
+ */
+#ifndef HSA_H
+#define HSA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define HSA_API __attribute__((visibility("default")))
+#else
+#define HSA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *hsa_stream_t; /* identical to cudaStream_t */
+
+typedef enum {
+    HSA_OK = 0,
+    HSA_ERR_INVALID_ARG = 1, /* a size, pointer or stride is invalid */
+    HSA_ERR_UNSUPPORTED = 2, /* valid but not supported: dtype, head dim, alignment, device */
+    HSA_ERR_WORKSPACE = 3,   /* workspace missing or too small */
+    HSA_ERR_CUDA = 4,        /* a CUDA runtime call failed (message in hsa_last_error) */
+    HSA_ERR_DEVICE_FLAG = 5  /* a kernel raised its range-violation flag (hsa_check) */
+} hsa_status_t;
+
+typedef enum {
+    HSA_F32 = 0, /* IEEE fp32 */
+    HSA_BF16 = 1 /* bfloat16 */
+} hsa_dtype_t;
+
+/* Thread-local, NUL-terminated message describing the last failure on this
+ * thread ("" if none).  The pointer stays valid until the next call on this
+ * thread. */
+HSA_API const char *hsa_last_error(void);
+
+/* Library ABI version (major*10000 + minor*100 + patch). */
+HSA_API int hsa_version(void);
+
+/* Synchronises `stream`, then reports (and clears) any pending asynchronous
+ * CUDA error and the device range-violation flag of the current device. */
+HSA_API hsa_status_t hsa_check(hsa_stream_t stream);
+
+/*
+ * hsa_compress -- KV compression (QbitAI article, 混合注意力机制: CSA step 1
+ * "every m tokens' KV entries are merged into one"; HCA "every m' = 128 tokens
+ * into one, no overlap").
+ *   kc[b, j, :] = sum_{r<m} w[r] * k[b, j*m + r, :]   (and vc from v)
+ * for every block j in [tok_begin[b] / m, tok_end[b] / m) (integer division),
+ * accumulated in fp32 in the order r = 0..m-1 and rounded once (RNE) to `dt`.
+ *   k, v       [B, N_cap, d] of `dt`, strides (in_sb, in_st), unit channel stride
+ *   tok_begin, tok_end  device int64 [B]; 0 <= tok_begin <= tok_end <= N_cap
+ *   max_blocks host bound on tok_end/m - tok_begin/m over all b (grid size)
+ *   w          device fp32 [m]; weights (normally summing to 1)
+ *   kc, vc     [B, E_cap, d] of `dt`, strides (out_sb, out_se); may alias
+ *              nothing that k/v reads
+ * m in [1, 4096], d a multiple of 8 (bf16) or 4 (fp32), d <= 512.
+ * Blocks beyond N_cap or E_cap are skipped and raise the device flag.
+ */
+HSA_API hsa_status_t hsa_compress(const void *k, const void *v, hsa_dtype_t dt, int B, int d,
+                          int64_t in_sb, int64_t in_st, int64_t N_cap,
+                          const int64_t *tok_begin, const int64_t *tok_end, int64_t max_blocks,
+                          const float *w, int m,
+                          void *kc, void *vc, int64_t out_sb, int64_t out_se, int64_t E_cap,
+                          hsa_stream_t stream);
+
+/*
+ * hsa_index_topk -- lightning indexer and exact top-k (QbitAI article,
+ * 混合注意力机制: CSA step 2 "a light indexer scores each query token against
+ * every compressed block, the top-k blocks are kept"; k = 512 for V4-Flash and
+ * 1024 for V4-Pro per the yage.ai essay on agentic workloads).
+ * For query t of sequence b at position p = q_pos0[b] + t:
+ *   s_j = sum_c q_idx[b, t, c] * k_idx[b, j, c]   (exact int32)
+ * for the E(p) = floor((p+1)/m) visible entries; the first min(topk, E(p)) of
+ * j ordered by (s_j desc, j asc) are written to idx_out[b, t, :] in ASCENDING
+ * index order, padded with -1; cnt_out[b, t] = min(topk, E(p)).
+ *   q_idx      int8 [B, T, DI], strides (q_sb, q_st)
+ *   k_idx      int8 [B, E_cap, DI], strides (k_sb, k_se); E(p) <= E_cap required
+ *   q_pos0     device int64 [B]
+ *   idx_out    int32 [B, T, topk] contiguous;  cnt_out int32 [B, T] contiguous
+ *   ws         workspace of hsa_index_topk_workspace_size bytes
+ * DI a multiple of 16 in [16, 128]; 1 <= topk <= 4096; m >= 1.
+ * Results are bit-identical for every input (ties included) and independent
+ * of B, T and the launch configuration.
+ */
+HSA_API hsa_status_t hsa_index_topk_workspace_size(int B, int T, int DI, int64_t E_cap, int topk,
+                                           size_t *bytes);
+HSA_API hsa_status_t hsa_index_topk(const int8_t *q_idx, int64_t q_sb, int64_t q_st,
+                            const int8_t *k_idx, int64_t k_sb, int64_t k_se, int64_t E_cap,
+                            int B, int T, int DI, const int64_t *q_pos0, int m, int topk,
+                            int32_t *idx_out, int32_t *cnt_out, void *ws, size_t ws_bytes,
+                            hsa_stream_t stream);
+
+/*
+ * hsa_attn_decode -- one new query token per sequence (QbitAI article,
+ * 混合注意力机制: CSA step 3, MQA over the selected compressed entries; HCA,
+ * dense over all entries; the sliding-window paragraph: the most recent
+ * `window` raw tokens, current one included, join the same softmax).
+ * Sequence b's query sits at p = ctx_len[b] - 1 and attends, per head h, to
+ *   S = {kc/vc[b, j] : j in idx[b, :cnt[b]]}  (CSA)  or  {j < E(p)}  (HCA: idx == NULL)
+ *     + {k_raw/v_raw[b, t] : max(0, p-window+1) <= t <= p}
+ * with logits scale * <q[b,h], k_x> and one softmax; out[b, h] is the
+ * softmax-weighted sum of v_x and lse[b, h] its natural-log normaliser
+ * (-inf and out = 0 for an empty set).  Work is split over the set and the
+ * parts are combined with the log-sum-exp rule; the split count of a
+ * sequence depends only on its own set size.
+ *   q          [B, H, d] of `dt`, contiguous
+ *   kc, vc     [B, E_cap, d] of `dt`, strides (c_sb, c_se)
+ *   idx, cnt   int32 [B, topk] (ascending or not; entries < 0 are skipped)
+ *              and int32 [B] (NULL: all topk slots are scanned), or idx = NULL
+ *              for dense HCA
+ *   k_raw, v_raw [B, N_cap, d] of `dt`, strides (r_sb, r_st)
+ *   ctx_len    device int64 [B]; 1 <= ctx_len <= N_cap
+ *   out        [B, H, d] of `dt`, contiguous;  lse fp32 [B, H] or NULL
+ *   ws         workspace of hsa_attn_decode_workspace_size bytes
+ * bf16: d in {64, 128}, H a multiple of 16 up to 128.  fp32: d a multiple of
+ * 32 up to 256, any H.
+ */
+HSA_API hsa_status_t hsa_attn_decode_workspace_size(hsa_dtype_t dt, int B, int H, int d, int64_t E_cap,
+                                            int m, int topk, int window, size_t *bytes);
+HSA_API hsa_status_t hsa_attn_decode(const void *q, hsa_dtype_t dt, int B, int H, int d,
+                             const void *kc, const void *vc, int64_t c_sb, int64_t c_se,
+                             int64_t E_cap, int m, const int32_t *idx, const int32_t *cnt, int topk,
+                             const void *k_raw, const void *v_raw, int64_t r_sb, int64_t r_st,
+                             int64_t N_cap, int window, const int64_t *ctx_len, float scale,
+                             void *out, float *lse, void *ws, size_t ws_bytes, hsa_stream_t stream);
+
+/*
+ * hsa_attn_prefill -- T query tokens per sequence at positions
+ * q_pos0[b] .. q_pos0[b]+T-1, each with its own set S as in hsa_attn_decode
+ * (causal within the chunk through E(p) and the window bound; the raw cache
+ * already holds every query token).
+ *   q          [B, T, H, d] of `dt`, contiguous
+ *   idx, cnt   int32 [B, T, topk] and [B, T] (cnt may be NULL), or idx = NULL (HCA)
+ *   out        [B, T, H, d] of `dt`;  lse fp32 [B, T, H] or NULL
+ * Other arguments as hsa_attn_decode.
+ */
+HSA_API hsa_status_t hsa_attn_prefill_workspace_size(hsa_dtype_t dt, int B, int T, int H, int d,
+                                             int64_t E_cap, int m, int topk, int window,
+                                             size_t *bytes);
+HSA_API hsa_status_t hsa_attn_prefill(const void *q, hsa_dtype_t dt, int B, int T, int H, int d,
+                              const void *kc, const void *vc, int64_t c_sb, int64_t c_se,
+                              int64_t E_cap, int m, const int32_t *idx, const int32_t *cnt, int topk,
+                              const void *k_raw, const void *v_raw, int64_t r_sb, int64_t r_st,
+                              int64_t N_cap, int window, const int64_t *q_pos0, float scale,
+                              void *out, float *lse, void *ws, size_t ws_bytes,
+                              hsa_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* HSA_H */

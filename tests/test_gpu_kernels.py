@@ -1,0 +1,292 @@
+"""GPU parity of each kernel against the CPU oracle, on seeded inputs at sizes
+the oracle finishes in seconds that still span several tiles, chunks and splits
+and end in ragged tails, plus the degenerate cases of the method."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from hsa_testlib import (assert_close_lse, assert_close_out, gpu_compress, gpu_index, host_np, scale_of)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    from compressed_attention_compress_b300 import _lib
+    return _lib
+
+
+def _randn(shape, seed, dtype=torch.bfloat16):
+    g = torch.Generator().manual_seed(seed)
+    return torch.randn(shape, generator=g).to(dtype)
+
+
+def _randint8(shape, seed, lo=-127, hi=127):
+    g = torch.Generator().manual_seed(seed)
+    return torch.randint(lo, hi + 1, shape, generator=g, dtype=torch.int16).to(torch.int8)
+
+
+# ------------------------------------------------------------- compressor ---
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("m", [1, 4, 5, 128])
+def test_compress_parity(lib, dtype, m):
+    B, N, d = 3, 37 * m + 3, 128 if dtype == torch.bfloat16 else 64
+    k = _randn((B, N, d), 11 + m, dtype)
+    v = _randn((B, N, d), 12 + m, dtype)
+    g = torch.Generator().manual_seed(13)
+    w = (1.0 - torch.rand(m, generator=g, dtype=torch.float64))
+    w = (w / w.sum()).float()
+    E_cap = N // m
+    tb, te = [0, 2 * m + 1, 5], [N, N - 1, 9 * m]
+    kc, vc = gpu_compress(k.cuda(), v.cuda(), w, m, tb, te, E_cap, lib)
+    torch.cuda.synchronize()
+    ok = oracle.compress(host_np(k), w.numpy(), m, tb, te, E_cap)
+    ov = oracle.compress(host_np(v), w.numpy(), m, tb, te, E_cap)
+    for gpu, ref in ((kc, ok), (vc, ov)):
+        g_ = gpu.float().cpu().numpy().astype(np.float64)
+        if dtype == torch.bfloat16:
+            tol = np.abs(ref) * 2.0 ** -8 + 2.0 ** -24 * m
+        else:
+            tol = np.abs(ref) * 1e-6 + 1e-6
+        assert (np.abs(g_ - ref) <= tol).all()
+    lib.hsa_check()
+
+
+@pytest.mark.parametrize("m", [4, 128])
+def test_compress_one_hot_bit_exact(lib, m):
+    B, N, d = 2, 9 * m, 128
+    k = _randn((B, N, d), 21)
+    v = _randn((B, N, d), 22)
+    for r0 in (0, m - 1):
+        w = torch.zeros(m)
+        w[r0] = 1.0
+        kc, vc = gpu_compress(k.cuda(), v.cuda(), w, m, [0, 0], [N, N], N // m, lib)
+        assert torch.equal(kc.cpu(), k[:, r0::m][:, :N // m])
+        assert torch.equal(vc.cpu(), v[:, r0::m][:, :N // m])
+
+
+# ------------------------------------------------------------------ top-k ---
+
+def _index_case(lib, B, T, E_cap, DI, m, topk, pos0, lo=-127, hi=127, seed=0, k_idx=None):
+    q = _randint8((B, T, DI), 100 + seed, lo, hi)
+    kI = _randint8((B, E_cap, DI), 200 + seed, lo, hi) if k_idx is None else k_idx
+    pos0_t = torch.tensor(pos0, dtype=torch.int64)
+    idx, cnt = gpu_index(q.cuda(), kI.cuda(), pos0_t, m, topk, lib)
+    torch.cuda.synchronize()
+    rows_b = np.repeat(np.arange(B), T)
+    rows_p = (np.asarray(pos0)[:, None] + np.arange(T)[None, :]).reshape(-1)
+    oi, oc = oracle.index_topk_rows(q.numpy().reshape(B * T, DI), rows_b, rows_p, kI.numpy(), m, topk)
+    assert np.array_equal(cnt.cpu().numpy().reshape(-1), oc)
+    assert np.array_equal(idx.cpu().numpy().reshape(B * T, topk), oi)
+    lib.hsa_check()
+
+
+@pytest.mark.parametrize("DI", [16, 32, 64, 128])
+def test_index_topk_random(lib, DI):
+    E_cap = 9000 + 37
+    _index_case(lib, B=3, T=1, E_cap=E_cap, DI=DI, m=4, topk=300,
+                pos0=[4 * E_cap - 1, 4 * 5000 + 2, 4 * E_cap - 3], seed=DI)
+
+
+@pytest.mark.parametrize("topk", [1, 64, 512, 1024, 2048])
+def test_index_topk_k_sizes(lib, topk):
+    E_cap = 40000
+    _index_case(lib, B=2, T=1, E_cap=E_cap, DI=64, m=4, topk=topk, pos0=[4 * E_cap - 1, 4 * 31111], seed=topk)
+
+
+def test_index_topk_short_rows_and_empty(lib):
+    # E(p) < k, E(p) = 0 (p < m - 1), exactly one entry
+    _index_case(lib, B=5, T=1, E_cap=600, DI=64, m=4, topk=512, pos0=[0, 2, 3, 4 * 100 + 1, 4 * 600 - 1], seed=7)
+
+
+def test_index_topk_heavy_ties_fast_and_fallback(lib):
+    # values in {-1, 0, 1}: every score in one level-1 bin -> the fallback pass
+    _index_case(lib, B=2, T=1, E_cap=30000, DI=64, m=4, topk=1024, pos0=[4 * 30000 - 1, 4 * 2000], lo=-1, hi=1, seed=3)
+    # all-equal scores: lowest indices
+    z = torch.zeros((1, 20000, 64), dtype=torch.int8)
+    _index_case(lib, B=1, T=1, E_cap=20000, DI=64, m=4, topk=777, pos0=[4 * 20000 - 1], k_idx=z, seed=4)
+
+
+def test_index_topk_extreme_values(lib):
+    # -128 everywhere: largest possible scores, all tied
+    kI = torch.full((1, 5000, 64), -128, dtype=torch.int8)
+    kI[0, 4000:4100] = 127
+    _index_case(lib, B=1, T=1, E_cap=5000, DI=64, m=4, topk=200, pos0=[4 * 5000 - 1], lo=-128, hi=-128, k_idx=kI)
+
+
+def test_index_topk_multi_query_prefill_rows(lib):
+    E_cap = 3000
+    _index_case(lib, B=2, T=37, E_cap=E_cap, DI=64, m=4, topk=128, pos0=[4 * E_cap - 37, 200], seed=9)
+
+
+def test_index_topk_planted(lib):
+    E_cap, DI, k = 50000, 64, 256
+    q = _randint8((1, 1, DI), 5)
+    kI = _randint8((1, E_cap, DI), 6, -3, 3)
+    g = torch.Generator().manual_seed(7)
+    planted = torch.randperm(E_cap, generator=g)[:k].sort().values
+    kI[0, planted] = q[0, 0]
+    idx, cnt = gpu_index(q.cuda(), kI.cuda(), torch.tensor([4 * E_cap - 1]), 4, k, lib)
+    assert torch.equal(idx.cpu()[0, 0].long(), planted)
+    assert int(cnt[0, 0]) == k
+
+
+# -------------------------------------------------------------- attention ---
+
+def _attn_inputs(B, E_cap, N, H, d, dtype, seed):
+    return (_randn((B, E_cap, d), seed + 1, dtype), _randn((B, E_cap, d), seed + 2, dtype),
+            _randn((B, N, d), seed + 3, dtype), _randn((B, N, d), seed + 4, dtype))
+
+
+def _random_idx(rows_E, topk, seed):
+    g = np.random.default_rng(seed)
+    idx = np.full((len(rows_E), topk), -1, np.int32)
+    cnt = np.zeros(len(rows_E), np.int32)
+    for r, E in enumerate(rows_E):
+        n = min(topk, E)
+        sel = np.sort(g.choice(E, size=n, replace=False)) if n else np.zeros(0, np.int64)
+        idx[r, :n] = sel
+        cnt[r] = n
+    return idx, cnt
+
+
+@pytest.mark.parametrize("dtype,H,d", [(torch.bfloat16, 64, 128), (torch.bfloat16, 128, 128),
+                                       (torch.bfloat16, 16, 64), (torch.float32, 8, 64)])
+@pytest.mark.parametrize("dense", [False, True])
+def test_attn_decode_parity(lib, dtype, H, d, dense):
+    B, m, W, topk = 5, 4, 128, 300
+    ctx = [4 * 2000, 4 * 1500 + 3, 130, 1, 77]
+    N = max(ctx)
+    E_cap = N // m
+    kc, vc, kr, vr = _attn_inputs(B, E_cap, N, H, d, dtype, 40)
+    q = _randn((B, H, d), 44, dtype)
+    rows_p = np.asarray(ctx) - 1
+    rows_E = [(p + 1) // m for p in rows_p]
+    if dense:
+        idx = cnt = None
+    else:
+        idx, cnt = _random_idx(rows_E, topk, 45)
+    out = torch.empty((B, H, d), dtype=dtype, device="cuda")
+    lse = torch.empty((B, H), dtype=torch.float32, device="cuda")
+    ws = lib.workspace(lib.hsa_attn_decode_workspace_size(dtype, B, H, d, E_cap, m, 0 if dense else topk, W))
+    lib.hsa_attn_decode(q.cuda(), kc.cuda(), vc.cuda(), m,
+                        None if dense else torch.from_numpy(idx).cuda(),
+                        None if dense else torch.from_numpy(cnt).cuda(),
+                        kr.cuda(), vr.cuda(), W, torch.tensor(ctx).cuda(), scale_of(d), out, lse, ws)
+    torch.cuda.synchronize()
+    ro, rl = oracle.attn_rows(host_np(q), np.arange(B), rows_p, host_np(kc), host_np(vc), m, idx,
+                              host_np(kr), host_np(vr), W, scale_of(d))
+    assert_close_out(out, ro, dtype)
+    assert_close_lse(lse, rl)
+    lib.hsa_check()
+
+
+def test_attn_decode_without_cnt_and_unsorted_idx(lib):
+    B, H, d, m, W, topk = 2, 64, 128, 4, 128, 200
+    N = 4 * 3000
+    E_cap = N // m
+    kc, vc, kr, vr = _attn_inputs(B, E_cap, N, H, d, torch.bfloat16, 50)
+    q = _randn((B, H, d), 54)
+    idx, _ = _random_idx([E_cap, 150], topk, 55)
+    idx = np.ascontiguousarray(idx[:, ::-1])  # padding first, descending: any order is allowed
+    out = torch.empty((B, H, d), dtype=torch.bfloat16, device="cuda")
+    ws = lib.workspace(lib.hsa_attn_decode_workspace_size(torch.bfloat16, B, H, d, E_cap, m, topk, W))
+    ctx = [N, 4 * 150 + 3]
+    lib.hsa_attn_decode(q.cuda(), kc.cuda(), vc.cuda(), m, torch.from_numpy(idx).cuda(), None, kr.cuda(), vr.cuda(),
+                        W, torch.tensor(ctx).cuda(), scale_of(d), out, None, ws)
+    ro, _ = oracle.attn_rows(host_np(q), np.arange(B), np.asarray(ctx) - 1, host_np(kc), host_np(vc), m, idx,
+                             host_np(kr), host_np(vr), W, scale_of(d))
+    assert_close_out(out, ro, torch.bfloat16)
+
+
+def test_attn_decode_window_only_and_empty(lib):
+    # k = 0 (all -1) -> sliding-window attention; window 0 + no entries -> empty set
+    B, H, d, m = 2, 16, 128, 4
+    N = 500
+    kc, vc, kr, vr = _attn_inputs(B, N // m, N, H, d, torch.bfloat16, 60)
+    q = _randn((B, H, d), 64)
+    for W in (128, 0):
+        idx = np.full((B, 8), -1, np.int32)
+        out = torch.empty((B, H, d), dtype=torch.bfloat16, device="cuda")
+        lse = torch.empty((B, H), dtype=torch.float32, device="cuda")
+        ws = lib.workspace(lib.hsa_attn_decode_workspace_size(torch.bfloat16, B, H, d, N // m, m, 8, W))
+        ctx = [N, 50]
+        lib.hsa_attn_decode(q.cuda(), kc.cuda(), vc.cuda(), m, torch.from_numpy(idx).cuda(), None, kr.cuda(),
+                            vr.cuda(), W, torch.tensor(ctx).cuda(), scale_of(d), out, lse, ws)
+        ro, rl = oracle.attn_rows(host_np(q), np.arange(B), np.asarray(ctx) - 1, host_np(kc), host_np(vc), m, idx,
+                                  host_np(kr), host_np(vr), W, scale_of(d))
+        assert_close_out(out, ro, torch.bfloat16)
+        assert_close_lse(lse, rl)
+
+
+@pytest.mark.parametrize("dtype,H,d", [(torch.bfloat16, 64, 128), (torch.float32, 8, 64)])
+@pytest.mark.parametrize("dense", [False, True])
+def test_attn_prefill_parity(lib, dtype, H, d, dense):
+    B, T, m, W, topk = 2, 70, 4, 128, 96
+    pos0 = [4 * 700 - 70, 9]
+    N = 4 * 700
+    E_cap = N // m
+    kc, vc, kr, vr = _attn_inputs(B, E_cap, N, H, d, dtype, 70)
+    q = _randn((B, T, H, d), 74, dtype)
+    rows_p = (np.asarray(pos0)[:, None] + np.arange(T)[None, :]).reshape(-1)
+    rows_b = np.repeat(np.arange(B), T)
+    rows_E = [(p + 1) // m for p in rows_p]
+    if dense:
+        idx = cnt = None
+    else:
+        idx, cnt = _random_idx(rows_E, topk, 75)
+    out = torch.empty((B, T, H, d), dtype=dtype, device="cuda")
+    lse = torch.empty((B, T, H), dtype=torch.float32, device="cuda")
+    lib.hsa_attn_prefill(q.cuda(), kc.cuda(), vc.cuda(), m,
+                         None if dense else torch.from_numpy(idx.reshape(B, T, topk)).cuda(),
+                         None if dense else torch.from_numpy(cnt.reshape(B, T)).cuda(),
+                         kr.cuda(), vr.cuda(), W, torch.tensor(pos0).cuda(), scale_of(d), out, lse)
+    torch.cuda.synchronize()
+    ro, rl = oracle.attn_rows(host_np(q.reshape(B * T, H, d)), rows_b, rows_p, host_np(kc), host_np(vc), m, idx,
+                              host_np(kr), host_np(vr), W, scale_of(d))
+    assert_close_out(out.reshape(B * T, H, d), ro, dtype)
+    assert_close_lse(lse.reshape(B * T, H), rl)
+    lib.hsa_check()
+
+
+# ---------------------------------------------------------- error paths ---
+
+def test_errors_leave_stream_usable(lib):
+    B, H, d, m, W = 1, 16, 128, 4, 16
+    N = 256
+    kc, vc, kr, vr = [t.cuda() for t in _attn_inputs(B, N // m, N, H, d, torch.bfloat16, 80)]
+    q = _randn((B, H, d), 84).cuda()
+    out = torch.empty((B, H, d), dtype=torch.bfloat16, device="cuda")
+    ctx = torch.tensor([N]).cuda()
+    idx = torch.tensor([[1, 2, 3]], dtype=torch.int32).cuda()
+    need = lib.hsa_attn_decode_workspace_size(torch.bfloat16, B, H, d, N // m, m, 3, W)
+    if need:
+        with pytest.raises(lib.HSAError) as ei:
+            lib.hsa_attn_decode(q, kc, vc, m, idx, None, kr, vr, W, ctx, 0.1, out, None, lib.workspace(need - 1))
+        assert ei.value.status == lib.HSA_ERR_WORKSPACE
+    with pytest.raises(lib.HSAError) as ei:  # d not supported on the bf16 path
+        lib.hsa_attn_decode(q[..., :96].contiguous(), kc[..., :96].contiguous(), vc[..., :96].contiguous(), m, idx,
+                            None, kr[..., :96].contiguous(), vr[..., :96].contiguous(), W, ctx, 0.1,
+                            out[..., :96].contiguous(), None, lib.workspace(max(need, 1)))
+    assert ei.value.status == lib.HSA_ERR_UNSUPPORTED
+    with pytest.raises(lib.HSAError) as ei:  # topk out of range
+        lib.hsa_index_topk(torch.zeros((1, 1, 64), dtype=torch.int8, device="cuda"),
+                           torch.zeros((1, 10, 64), dtype=torch.int8, device="cuda"), torch.tensor([39]).cuda(), 4,
+                           5000, torch.empty((1, 1, 5000), dtype=torch.int32, device="cuda"),
+                           torch.empty((1, 1), dtype=torch.int32, device="cuda"), None)
+    assert ei.value.status == lib.HSA_ERR_UNSUPPORTED
+    # a selected index beyond E(p) is skipped and flagged, never read
+    bad = torch.tensor([[1, N // m + 5, 3]], dtype=torch.int32).cuda()
+    lib.hsa_attn_decode(q, kc, vc, m, bad, None, kr, vr, W, ctx, 0.1, out, None, lib.workspace(max(need, 1)))
+    with pytest.raises(lib.HSAError) as ei:
+        lib.hsa_check()
+    assert ei.value.status == lib.HSA_ERR_DEVICE_FLAG
+    # and the stream still works afterwards
+    lib.hsa_attn_decode(q, kc, vc, m, idx, None, kr, vr, W, ctx, 0.1, out, None, lib.workspace(max(need, 1)))
+    lib.hsa_check()
