@@ -313,8 +313,8 @@ __global__ void __launch_bounds__(NW * 32) attn_bf16_kernel(AttnArgs a) {
 template <int D, int NT, int NW>
 cudaError_t launch_bf16_t(const AttnArgs &a, cudaStream_t s) {
     const size_t smem = (size_t)NW * 16 * D * 2 + 4 * (size_t)NT * D * 2 + 2 * NT * sizeof(int64_t) + 2 * NT;
-    cudaError_t e = cudaFuncSetAttribute(attn_bf16_kernel<D, NT, NW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
+    static unsigned long long done = 0;
+    cudaError_t e = smem_limit_once(attn_bf16_kernel<D, NT, NW>, (int)smem, done);
     if (e != cudaSuccess) return e;
     const int splits = a.split > 0 ? a.max_splits : 1;
     dim3 grid(splits, a.rows);
@@ -405,47 +405,58 @@ __global__ void __launch_bounds__(128) attn_f32_kernel(AttnArgs a) {
 }
 
 // ------------------------------------------------------------ split merge
-// out = sum_s exp(lse_s - lse) * o_s,  lse = ln sum_s exp(lse_s)  (rows with >1 split)
+// out = sum_s exp(lse_s - lse) * o_s,  lse = ln sum_s exp(lse_s)  (rows with >1 split).
+// One warp per (row, head): lanes own 4 channels each (d <= 128) and the split
+// weights are computed once per warp; the loads of all splits are independent.
 template <typename OutT>
-__global__ void __launch_bounds__(256) attn_merge_kernel(AttnArgs a) {
-    const int row = blockIdx.x;
+__global__ void __launch_bounds__(128) attn_merge_kernel(AttnArgs a) {
+    const int row = blockIdx.y;
+    const int h = blockIdx.x * 4 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (h >= a.H) return;
     const RowSet r = row_set(a, row);
     if (r.n_splits <= 1) return;
     const int D = a.d;
-    const int nq = D / 4;
-    for (int w = threadIdx.x; w < a.H * nq; w += blockDim.x) {
-        const int h = w / nq, c4 = w % nq;
-        const float *pl = a.part_lse + (int64_t)row * a.max_splits * a.H + h;
-        float M = -INFINITY;
-        for (int sp = 0; sp < r.n_splits; ++sp) M = fmaxf(M, pl[(int64_t)sp * a.H]);
+    const float *pl = a.part_lse + (int64_t)row * a.max_splits * a.H + h;
+    float M = -INFINITY;
+    for (int sp = lane; sp < r.n_splits; sp += 32) M = fmaxf(M, pl[(int64_t)sp * a.H]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    float L = 0.f;
+    for (int sp = lane; sp < r.n_splits; sp += 32) {
+        const float ls = pl[(int64_t)sp * a.H];
+        L += ls == -INFINITY ? 0.f : expf(ls - M);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+    const bool empty = M == -INFINITY || L == 0.f;
+    const float invL = empty ? 0.f : 1.f / L;
+    for (int c4 = lane; c4 < D / 4; c4 += 32) {
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        float L = 0.f;
-        if (M != -INFINITY) {
+        if (!empty) {
+            const float *po = a.part_o + ((int64_t)row * a.max_splits * a.H + h) * D + c4 * 4;
+#pragma unroll 4
             for (int sp = 0; sp < r.n_splits; ++sp) {
                 const float ls = pl[(int64_t)sp * a.H];
-                if (ls == -INFINITY) continue;
-                const float wgt = expf(ls - M);
-                L += wgt;
-                const float4 v = *reinterpret_cast<const float4 *>(
-                    a.part_o + (((int64_t)row * a.max_splits + sp) * a.H + h) * D + c4 * 4);
+                const float wgt = ls == -INFINITY ? 0.f : expf(ls - M) * invL;
+                const float4 v = *reinterpret_cast<const float4 *>(po + (int64_t)sp * a.H * D);
                 acc.x = fmaf(wgt, v.x, acc.x);
                 acc.y = fmaf(wgt, v.y, acc.y);
                 acc.z = fmaf(wgt, v.z, acc.z);
                 acc.w = fmaf(wgt, v.w, acc.w);
             }
         }
-        const float inv = L > 0.f ? 1.f / L : 0.f;
         OutT *out = static_cast<OutT *>(a.out) + ((int64_t)row * a.H + h) * D + c4 * 4;
         if constexpr (sizeof(OutT) == 2) {
             uint2 pk;
-            pk.x = pack_bf16x2(acc.x * inv, acc.y * inv);
-            pk.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+            pk.x = pack_bf16x2(acc.x, acc.y);
+            pk.y = pack_bf16x2(acc.z, acc.w);
             *reinterpret_cast<uint2 *>(out) = pk;
         } else {
-            *reinterpret_cast<float4 *>(out) = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+            *reinterpret_cast<float4 *>(out) = acc;
         }
-        if (a.lse && c4 == 0) a.lse[(int64_t)row * a.H + h] = L > 0.f ? M + logf(L) : -INFINITY;
     }
+    if (a.lse && lane == 0) a.lse[(int64_t)row * a.H + h] = empty ? -INFINITY : M + logf(L);
 }
 
 }  // namespace
@@ -487,10 +498,11 @@ cudaError_t launch_attn_f32(const AttnArgs &a, cudaStream_t s) {
 
 cudaError_t launch_attn_merge(const AttnArgs &a, bool bf16, cudaStream_t s) {
     if (a.split <= 0) return cudaSuccess;
+    dim3 grid((a.H + 3) / 4, a.rows);
     if (bf16)
-        attn_merge_kernel<__nv_bfloat16><<<a.rows, 256, 0, s>>>(a);
+        attn_merge_kernel<__nv_bfloat16><<<grid, 128, 0, s>>>(a);
     else
-        attn_merge_kernel<float><<<a.rows, 256, 0, s>>>(a);
+        attn_merge_kernel<float><<<grid, 128, 0, s>>>(a);
     return cudaGetLastError();
 }
 

@@ -92,6 +92,12 @@ DecodePlan plan_decode(hsa_dtype_t dt, int B, int H, int d, int64_t E_cap, int m
                        bool dense, int num_sms) {
     DecodePlan p{};
     (void)m;
+    if (dt == HSA_BF16 && hsa::decode_cluster_supported(H, d)) {
+        p.split = -1;  // cluster kernel: splits live in one cluster, no workspace
+        p.max_splits = 1;
+        p.total = 0;
+        return p;
+    }
     const int64_t max_items = (dense ? E_cap : (int64_t)topk) + window;
     p.split = hsa::attn_split_size(dt == HSA_BF16, dense, H, B, max_items, num_sms);
     if (p.split <= 0) {
@@ -186,19 +192,49 @@ hsa_status_t hsa_compress(const void *k, const void *v, hsa_dtype_t dt, int B, i
                     "compress");
 }
 
+}  // extern "C"
+
+namespace {
+// Decode-shaped calls (all CTAs of the rows resident at once) take the fused
+// cooperative kernel; larger row counts take the two-kernel path in groups.
+struct IndexChoice {
+    bool fused;
+    hsa::FusedIndexPlan fp;
+    hsa::IndexPlan tp;
+    int group;
+    size_t bytes;
+};
+IndexChoice choose_index(int rows, int DI, int64_t E_cap, int topk, int num_sms) {
+    IndexChoice c{};
+    c.fp = hsa::plan_index_fused(rows, DI, E_cap, num_sms);
+    if (c.fp.ok) {
+        c.fused = true;
+        c.bytes = c.fp.total;
+        return c;
+    }
+    c.group = index_group_rows(rows, E_cap);
+    c.tp = hsa::plan_index(c.group, DI, E_cap, topk, num_sms);
+    c.bytes = c.tp.total;
+    return c;
+}
+}  // namespace
+
+extern "C" {
+
 hsa_status_t hsa_index_topk_workspace_size(int B, int T, int DI, int64_t E_cap, int topk, size_t *bytes) {
     if (!bytes) return fail(HSA_ERR_INVALID_ARG, "null bytes");
     if (B < 0 || T < 0 || E_cap < 0 || topk <= 0 || DI <= 0) return fail(HSA_ERR_INVALID_ARG, "bad size");
+    if (DI != 16 && DI != 32 && DI != 64 && DI != 128)
+        return fail(HSA_ERR_UNSUPPORTED, "indexer dim must be 16, 32, 64 or 128, got %d", DI);
     DevInfo di;
     hsa_status_t st = device_info(di);
     if (st != HSA_OK) return st;
     const int rows = B * T;
-    if (rows == 0) {
+    if (rows == 0 || E_cap == 0) {
         *bytes = 0;
         return ok();
     }
-    const hsa::IndexPlan p = hsa::plan_index(index_group_rows(rows, E_cap), DI, E_cap, topk, di.num_sms);
-    *bytes = p.total;
+    *bytes = choose_index(rows, DI, E_cap, topk, di.num_sms).bytes;
     return ok();
 }
 
@@ -219,22 +255,23 @@ hsa_status_t hsa_index_topk(const int8_t *q_idx, int64_t q_sb, int64_t q_st, con
     DevInfo di;
     hsa_status_t st = device_info(di);
     if (st != HSA_OK) return st;
-    const int G = index_group_rows(rows, E_cap);
-    const hsa::IndexPlan p = hsa::plan_index(G, DI, E_cap, topk, di.num_sms);
-    if (!ws || ws_bytes < p.total)
-        return fail(HSA_ERR_WORKSPACE, "index workspace needs %zu bytes, got %zu", p.total, ws_bytes);
-    if ((reinterpret_cast<uintptr_t>(ws) & 255) != 0) return fail(HSA_ERR_WORKSPACE, "workspace must be 256-byte aligned");
-    if ((st = pending_error()) != HSA_OK) return st;
     hsa::IndexArgs a{q_idx, q_sb, q_st, k_idx, k_sb, k_se, E_cap, B, T, DI, q_pos0, m, topk, idx_out, cnt_out};
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (E_cap == 0) {
         // no entry can be visible: everything is padding
+        if ((st = pending_error()) != HSA_OK) return st;
         cudaError_t e = cudaMemsetAsync(idx_out, 0xff, sizeof(int32_t) * (size_t)rows * topk, s);
         if (e == cudaSuccess) e = cudaMemsetAsync(cnt_out, 0, sizeof(int32_t) * (size_t)rows, s);
         return launched(e, "index (empty)");
     }
-    for (int r0 = 0; r0 < rows; r0 += G) {
-        cudaError_t e = hsa::launch_index_topk(a, p, ws, r0, s);
+    const IndexChoice ch = choose_index(rows, DI, E_cap, topk, di.num_sms);
+    if (!ws || ws_bytes < ch.bytes)
+        return fail(HSA_ERR_WORKSPACE, "index workspace needs %zu bytes, got %zu", ch.bytes, ws_bytes);
+    if ((reinterpret_cast<uintptr_t>(ws) & 255) != 0) return fail(HSA_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+    if ((st = pending_error()) != HSA_OK) return st;
+    if (ch.fused) return launched(hsa::launch_index_fused(a, ch.fp, ws, s), "index_topk (fused)");
+    for (int r0 = 0; r0 < rows; r0 += ch.group) {
+        cudaError_t e = hsa::launch_index_topk(a, ch.tp, ws, r0, s);
         if (e != cudaSuccess) return launched(e, "index_topk");
     }
     return ok();
@@ -281,6 +318,7 @@ hsa_status_t hsa_attn_decode(const void *q, hsa_dtype_t dt, int B, int H, int d,
     a.part_o = p.total ? reinterpret_cast<float *>(static_cast<char *>(ws) + p.off_o) : nullptr;
     a.part_lse = p.total ? reinterpret_cast<float *>(static_cast<char *>(ws) + p.off_lse) : nullptr;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (p.split < 0) return launched(hsa::launch_attn_decode_cluster(a, s), "attn_decode (cluster)");
     cudaError_t e = dt == HSA_BF16 ? hsa::launch_attn_bf16(a, s) : hsa::launch_attn_f32(a, s);
     if (e != cudaSuccess) return launched(e, "attn_decode");
     return launched(hsa::launch_attn_merge(a, dt == HSA_BF16, s), "attn_merge");

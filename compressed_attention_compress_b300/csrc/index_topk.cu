@@ -471,12 +471,9 @@ static cudaError_t launch_lpe(const IndexArgs &a, const IndexPlan &p, void *ws, 
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const size_t smem = collect_smem(p);
-    static bool attr_set = false;
-    if (!attr_set) {
-        e = cudaFuncSetAttribute(index_collect_kernel<LPE>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
+    static unsigned long long done = 0;
+    e = smem_limit_once(index_collect_kernel<LPE>, 200 * 1024, done);
+    if (e != cudaSuccess) return e;
     index_collect_kernel<LPE><<<grid, kThreads, smem, s>>>(a, p, ws, row_begin);
     return cudaGetLastError();
 }

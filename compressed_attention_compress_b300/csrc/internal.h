@@ -45,6 +45,17 @@ IndexPlan plan_index(int rows, int DI, int64_t E_cap, int topk, int num_sms);
 cudaError_t launch_index_topk(const IndexArgs &a, const IndexPlan &p, void *ws, int row_begin,
                               cudaStream_t s);
 
+// Decode-shaped indexer: one cooperative launch (index_fused.cu).
+struct FusedIndexPlan {
+    bool ok;           // false: the rows do not fit one resident launch
+    int rows, ctas_per_row, chunk, key_bits, shift1, nb2, cap_in;
+    int off_stage_smem;  // byte offset of the copy stages in dynamic shared memory
+    size_t smem;
+    size_t off_hist1, off_bar, off_rec, off_in_u, off_in_j, off_keys, total;
+};
+FusedIndexPlan plan_index_fused(int rows, int DI, int64_t E_cap, int num_sms);
+cudaError_t launch_index_fused(const IndexArgs &a, const FusedIndexPlan &p, void *ws, cudaStream_t s);
+
 // -------------------------------------------------------------- attention
 struct AttnArgs {
     const void *q;      // [rows, H, d]
@@ -75,5 +86,8 @@ int attn_split_size(bool bf16, bool dense, int H, int rows, int64_t max_items, i
 cudaError_t launch_attn_bf16(const AttnArgs &a, cudaStream_t s);
 cudaError_t launch_attn_f32(const AttnArgs &a, cudaStream_t s);
 cudaError_t launch_attn_merge(const AttnArgs &a, bool bf16, cudaStream_t s);
+// bf16 decode with H in {16, 32, 64, 128}: one cluster per sequence, no workspace.
+bool decode_cluster_supported(int H, int d);
+cudaError_t launch_attn_decode_cluster(const AttnArgs &a, cudaStream_t s);
 
 }  // namespace hsa

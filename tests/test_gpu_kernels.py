@@ -290,3 +290,36 @@ def test_errors_leave_stream_usable(lib):
     # and the stream still works afterwards
     lib.hsa_attn_decode(q, kc, vc, m, idx, None, kr, vr, W, ctx, 0.1, out, None, lib.workspace(max(need, 1)))
     lib.hsa_check()
+
+
+@pytest.mark.parametrize("dense", [False, True])
+def test_attn_decode_batch_invariant(lib, dense):
+    # A sequence's decode output is bit-identical whatever else is in the batch:
+    # its work split depends only on its own set.
+    B, H, d, m, W, topk = 4, 128, 128, 4, 128, 256
+    ctx = [4 * 3000, 4 * 1200 + 1, 4 * 2500 + 2, 300]
+    N = max(ctx)
+    E_cap = N // m
+    kc, vc, kr, vr = [t.cuda() for t in _attn_inputs(B, E_cap, N, H, d, torch.bfloat16, 90)]
+    q = _randn((B, H, d), 94).cuda()
+    idx = cnt = None
+    if not dense:
+        i_np, c_np = _random_idx([(c - 1 + 1) // m for c in ctx], topk, 95)
+        idx, cnt = torch.from_numpy(i_np).cuda(), torch.from_numpy(c_np).cuda()
+
+    def run(sel):
+        bq = len(sel)
+        out = torch.empty((bq, H, d), dtype=torch.bfloat16, device="cuda")
+        lse = torch.empty((bq, H), dtype=torch.float32, device="cuda")
+        ws = lib.workspace(lib.hsa_attn_decode_workspace_size(torch.bfloat16, bq, H, d, E_cap, m,
+                                                              0 if dense else topk, W))
+        lib.hsa_attn_decode(q[sel].contiguous(), kc[sel].contiguous(), vc[sel].contiguous(), m,
+                            None if dense else idx[sel].contiguous(), None if dense else cnt[sel].contiguous(),
+                            kr[sel].contiguous(), vr[sel].contiguous(), W, torch.tensor(ctx).cuda()[sel], scale_of(d),
+                            out, lse, ws)
+        return out, lse
+
+    full_o, full_l = run([0, 1, 2, 3])
+    for i in range(B):
+        o1, l1 = run([i])
+        assert torch.equal(o1[0], full_o[i]) and torch.equal(l1[0], full_l[i])
