@@ -23,8 +23,9 @@ _STATUS = {0: "HSA_OK", 1: "HSA_ERR_INVALID_ARG", 2: "HSA_ERR_UNSUPPORTED", 3: "
 
 # every symbol include/hsa.h declares
 EXPORTS = ["hsa_last_error", "hsa_version", "hsa_check", "hsa_compress", "hsa_index_topk_workspace_size",
-           "hsa_index_topk", "hsa_attn_decode_workspace_size", "hsa_attn_decode",
+           "hsa_index_topk", "hsa_index_topk_noalloc", "hsa_attn_decode_workspace_size", "hsa_attn_decode",
            "hsa_attn_prefill_workspace_size", "hsa_attn_prefill"]
+NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
 class HSAError(RuntimeError):
@@ -49,6 +50,8 @@ def _load():
     lib.hsa_index_topk_workspace_size.argtypes = [I, I, I, I64, I, ctypes.POINTER(SZ)]
     lib.hsa_index_topk.restype = I
     lib.hsa_index_topk.argtypes = [P, I64, I64, P, I64, I64, I64, I, I, I, P, I, I, P, P, P, SZ, P]
+    lib.hsa_index_topk_noalloc.restype = I
+    lib.hsa_index_topk_noalloc.argtypes = [P, I64, I64, P, I64, I64, I64, I, I, I, P, I, I, P, P, P]
     lib.hsa_attn_decode_workspace_size.restype = I
     lib.hsa_attn_decode_workspace_size.argtypes = [I, I, I, I, I64, I, I, I, ctypes.POINTER(SZ)]
     lib.hsa_attn_decode.restype = I
@@ -114,6 +117,16 @@ def hsa_index_topk(q_idx, k_idx, q_pos0, m, topk, idx_out, cnt_out, ws, stream=N
     _chk(lib.hsa_index_topk(_p(q_idx), q_idx.stride(0), q_idx.stride(1), _p(k_idx), k_idx.stride(0), k_idx.stride(1),
                             E_cap, B, T, DI, _p(q_pos0), int(m), int(topk), _p(idx_out), _p(cnt_out), _p(ws),
                             ws.numel() * ws.element_size() if ws is not None else 0, _stream(stream)))
+
+
+def hsa_index_topk_noalloc(q_idx, k_idx, q_pos0, m, topk, idx_out, cnt_out, stream=None):
+    """hsa_index_topk without a workspace, for callers that cannot allocate device
+    memory: the library's built-in 16 MiB scratch is used instead.  Same result."""
+    B, T, DI = q_idx.shape
+    E_cap = k_idx.shape[1]
+    _chk(lib.hsa_index_topk_noalloc(_p(q_idx), q_idx.stride(0), q_idx.stride(1), _p(k_idx), k_idx.stride(0),
+                                    k_idx.stride(1), E_cap, B, T, DI, _p(q_pos0), int(m), int(topk), _p(idx_out),
+                                    _p(cnt_out), _stream(stream)))
 
 
 def hsa_attn_decode_workspace_size(dtype, B, H, d, E_cap, m, topk, window):

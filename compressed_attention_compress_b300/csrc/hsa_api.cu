@@ -5,6 +5,8 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <mutex>
+
 #include "../../include/hsa.h"
 #include "common.cuh"
 #include "internal.h"
@@ -360,3 +362,78 @@ hsa_status_t hsa_attn_prefill(const void *q, hsa_dtype_t dt, int B, int T, int H
 }
 
 }  // extern "C"
+
+// ------------------------------------------------------------------------
+// Allocation-free indexer: the scratch lives in this file-scope device array.
+// Host code never uses its name as an address; the device address is looked
+// up once per device with cudaGetSymbolAddress and passed to the kernels.
+namespace {
+static __device__ __align__(256) unsigned char g_noalloc_scratch[HSA_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void *g_noalloc_addr[kMaxDevices] = {};
+
+hsa_status_t noalloc_scratch(void **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail(HSA_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+    if (dev < 0 || dev >= kMaxDevices) return fail(HSA_ERR_UNSUPPORTED, "device ordinal %d above %d", dev, kMaxDevices);
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_addr[dev]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);  // with `dev` current
+        if (e != cudaSuccess || !p)
+            return fail(HSA_ERR_CUDA, "cudaGetSymbolAddress(scratch): %s", cudaGetErrorString(e));
+        g_noalloc_addr[dev] = p;
+    }
+    *out = g_noalloc_addr[dev];
+    return HSA_OK;
+}
+}  // namespace
+
+extern "C" hsa_status_t hsa_index_topk_noalloc(const int8_t *q_idx, int64_t q_sb, int64_t q_st, const int8_t *k_idx,
+                                               int64_t k_sb, int64_t k_se, int64_t E_cap, int B, int T, int DI,
+                                               const int64_t *q_pos0, int m, int topk, int32_t *idx_out,
+                                               int32_t *cnt_out, hsa_stream_t stream) {
+    if (B < 0 || T < 0 || E_cap < 0 || m <= 0) return fail(HSA_ERR_INVALID_ARG, "bad size");
+    if (topk <= 0 || topk > 4096) return fail(HSA_ERR_UNSUPPORTED, "topk must be in [1, 4096], got %d", topk);
+    if (DI != 16 && DI != 32 && DI != 64 && DI != 128)
+        return fail(HSA_ERR_UNSUPPORTED, "indexer dim must be 16, 32, 64 or 128, got %d", DI);
+    const int rows = B * T;
+    if (rows == 0) return ok();
+    if (!q_idx || !k_idx || !q_pos0 || !idx_out || !cnt_out) return fail(HSA_ERR_INVALID_ARG, "null pointer");
+    if (E_cap > (int64_t)1 << 30) return fail(HSA_ERR_UNSUPPORTED, "E_cap above 2^30");
+    if (!aligned16(q_idx) || !aligned16(k_idx) || q_sb % 16 || q_st % 16 || k_sb % 16 || k_se % 16)
+        return fail(HSA_ERR_UNSUPPORTED, "indexer tensors and strides must be 16-byte aligned");
+    if (k_se < DI || q_st < DI) return fail(HSA_ERR_INVALID_ARG, "indexer strides overlap rows");
+    DevInfo di;
+    hsa_status_t st = device_info(di);
+    if (st != HSA_OK) return st;
+    hsa::IndexArgs a{q_idx, q_sb, q_st, k_idx, k_sb, k_se, E_cap, B, T, DI, q_pos0, m, topk, idx_out, cnt_out};
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (E_cap == 0) {
+        if ((st = pending_error()) != HSA_OK) return st;
+        cudaError_t e = cudaMemsetAsync(idx_out, 0xff, sizeof(int32_t) * (size_t)rows * topk, s);
+        if (e == cudaSuccess) e = cudaMemsetAsync(cnt_out, 0, sizeof(int32_t) * (size_t)rows, s);
+        return launched(e, "index (empty)");
+    }
+    const IndexChoice ch = choose_index(rows, DI, E_cap, topk, di.num_sms);
+    if (ch.bytes > (size_t)HSA_NOALLOC_SCRATCH_BYTES)
+        return fail(HSA_ERR_WORKSPACE,
+                    "hsa_index_topk_noalloc: these sizes need %zu bytes of scratch, the built-in scratch holds %u; "
+                    "call hsa_index_topk with a workspace instead",
+                    ch.bytes, (unsigned)HSA_NOALLOC_SCRATCH_BYTES);
+    void *ws = nullptr;
+    if ((st = noalloc_scratch(&ws)) != HSA_OK) return st;
+    if ((st = pending_error()) != HSA_OK) return st;
+    // the array keeps the previous call's contents: zero what this call's kernels expect zeroed
+    cudaError_t e = cudaMemsetAsync(ws, 0, ch.bytes, s);
+    if (e != cudaSuccess) return launched(e, "index_topk_noalloc (clear scratch)");
+    if (ch.fused) return launched(hsa::launch_index_fused(a, ch.fp, ws, s), "index_topk_noalloc (fused)");
+    for (int r0 = 0; r0 < rows; r0 += ch.group) {
+        e = hsa::launch_index_topk(a, ch.tp, ws, r0, s);
+        if (e != cudaSuccess) return launched(e, "index_topk_noalloc");
+    }
+    return ok();
+}

@@ -136,6 +136,41 @@ HSA_API hsa_status_t hsa_index_topk(const int8_t *q_idx, int64_t q_sb, int64_t q
                             hsa_stream_t stream);
 
 /*
+ * hsa_index_topk_noalloc -- hsa_index_topk for callers that cannot allocate
+ * device memory.  The paper has no counterpart: this is a convenience of the
+ * library, not a step of the method.
+ *
+ * Some callers own every byte of device memory through their own pool (an
+ * inference server that reserves HBM up front, a framework whose caching
+ * allocator must see every allocation) or run where host code may not call
+ * cudaMalloc at all, and their interface hands this library only inputs and
+ * outputs, so they cannot pass the workspace hsa_index_topk needs.  This entry
+ * point takes the same arguments minus the workspace and computes the same
+ * result (bit-identical) in a scratch buffer built into the library: a static
+ * device array of HSA_NOALLOC_SCRATCH_BYTES (16 MiB) that every GPU which loads
+ * the library holds until the process exits.  It calls no cudaMalloc, cudaFree
+ * or allocating library routine.
+ *   - Calls whose scratch need (the value hsa_index_topk_workspace_size would
+ *     return for the same sizes) exceeds HSA_NOALLOC_SCRATCH_BYTES are rejected
+ *     with HSA_ERR_WORKSPACE and a message giving both sizes; use
+ *     hsa_index_topk with your own workspace for those.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before capturing a stream.
+ *   - Every call on a device shares the one array and it keeps the previous
+ *     call's contents; the call clears the part that must start at zero on its
+ *     stream before its kernels run.  Calls that overlap on the GPU (other
+ *     streams, other threads) race on the array: serialise them.
+ */
+#define HSA_NOALLOC_SCRATCH_BYTES (16u << 20)
+HSA_API hsa_status_t hsa_index_topk_noalloc(const int8_t *q_idx, int64_t q_sb, int64_t q_st,
+                                            const int8_t *k_idx, int64_t k_sb, int64_t k_se,
+                                            int64_t E_cap, int B, int T, int DI,
+                                            const int64_t *q_pos0, int m, int topk,
+                                            int32_t *idx_out, int32_t *cnt_out,
+                                            hsa_stream_t stream);
+
+/*
  * hsa_attn_decode -- one new query token per sequence (QbitAI article,
  * 混合注意力机制: CSA step 3, MQA over the selected compressed entries; HCA,
  * dense over all entries; the sliding-window paragraph: the most recent
