@@ -357,6 +357,8 @@ hsa_status_t hsa_attn_prefill(const void *q, hsa_dtype_t dt, int B, int T, int H
     a.pos = q_pos0; a.pos_is_ctx = 0; a.scale = scale; a.out = out; a.lse = lse;
     a.split = 0; a.max_splits = 1;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (dt == HSA_BF16 && hsa::prefill_tc_supported(a))
+        return launched(hsa::launch_attn_prefill_tc(a, di.num_sms, s), "attn_prefill (tcgen05)");
     cudaError_t e = dt == HSA_BF16 ? hsa::launch_attn_bf16(a, s) : hsa::launch_attn_f32(a, s);
     return launched(e, "attn_prefill");
 }

@@ -89,5 +89,8 @@ cudaError_t launch_attn_merge(const AttnArgs &a, bool bf16, cudaStream_t s);
 // bf16 decode with H in {16, 32, 64, 128}: one cluster per sequence, no workspace.
 bool decode_cluster_supported(int H, int d);
 cudaError_t launch_attn_decode_cluster(const AttnArgs &a, cudaStream_t s);
+// bf16 dense (HCA) prefill with d = 128 and T*H a multiple of 128: tcgen05 + TMA kernel.
+bool prefill_tc_supported(const AttnArgs &a);
+cudaError_t launch_attn_prefill_tc(const AttnArgs &a, int num_sms, cudaStream_t s);
 
 }  // namespace hsa
