@@ -200,18 +200,28 @@ namespace {
 // Decode-shaped calls (all CTAs of the rows resident at once) take the fused
 // cooperative kernel; larger row counts take the two-kernel path in groups.
 struct IndexChoice {
-    bool fused;
+    bool fused, prefill;
     hsa::FusedIndexPlan fp;
+    hsa::PrefillIndexPlan pp;
     hsa::IndexPlan tp;
     int group;
     size_t bytes;
 };
-IndexChoice choose_index(int rows, int DI, int64_t E_cap, int topk, int num_sms) {
+// Decode shapes take the fused cooperative kernel; many query rows per sequence
+// take the tensor-core path; what remains takes the two-kernel dp4a path.
+IndexChoice choose_index(int B, int T, int DI, int64_t E_cap, int topk, int num_sms) {
     IndexChoice c{};
+    const int rows = B * T;
     c.fp = hsa::plan_index_fused(rows, DI, E_cap, num_sms);
     if (c.fp.ok) {
         c.fused = true;
         c.bytes = c.fp.total;
+        return c;
+    }
+    c.pp = hsa::plan_index_prefill(B, T, DI, E_cap, topk, num_sms);
+    if (c.pp.ok) {
+        c.prefill = true;
+        c.bytes = c.pp.total;
         return c;
     }
     c.group = index_group_rows(rows, E_cap);
@@ -236,7 +246,7 @@ hsa_status_t hsa_index_topk_workspace_size(int B, int T, int DI, int64_t E_cap, 
         *bytes = 0;
         return ok();
     }
-    *bytes = choose_index(rows, DI, E_cap, topk, di.num_sms).bytes;
+    *bytes = choose_index(B, T, DI, E_cap, topk, di.num_sms).bytes;
     return ok();
 }
 
@@ -266,12 +276,13 @@ hsa_status_t hsa_index_topk(const int8_t *q_idx, int64_t q_sb, int64_t q_st, con
         if (e == cudaSuccess) e = cudaMemsetAsync(cnt_out, 0, sizeof(int32_t) * (size_t)rows, s);
         return launched(e, "index (empty)");
     }
-    const IndexChoice ch = choose_index(rows, DI, E_cap, topk, di.num_sms);
+    const IndexChoice ch = choose_index(B, T, DI, E_cap, topk, di.num_sms);
     if (!ws || ws_bytes < ch.bytes)
         return fail(HSA_ERR_WORKSPACE, "index workspace needs %zu bytes, got %zu", ch.bytes, ws_bytes);
     if ((reinterpret_cast<uintptr_t>(ws) & 255) != 0) return fail(HSA_ERR_WORKSPACE, "workspace must be 256-byte aligned");
     if ((st = pending_error()) != HSA_OK) return st;
     if (ch.fused) return launched(hsa::launch_index_fused(a, ch.fp, ws, s), "index_topk (fused)");
+    if (ch.prefill) return launched(hsa::launch_index_prefill(a, ch.pp, ws, di.num_sms, s), "index_topk (tensor cores)");
     for (int r0 = 0; r0 < rows; r0 += ch.group) {
         cudaError_t e = hsa::launch_index_topk(a, ch.tp, ws, r0, s);
         if (e != cudaSuccess) return launched(e, "index_topk");
@@ -420,7 +431,7 @@ extern "C" hsa_status_t hsa_index_topk_noalloc(const int8_t *q_idx, int64_t q_sb
         if (e == cudaSuccess) e = cudaMemsetAsync(cnt_out, 0, sizeof(int32_t) * (size_t)rows, s);
         return launched(e, "index (empty)");
     }
-    const IndexChoice ch = choose_index(rows, DI, E_cap, topk, di.num_sms);
+    const IndexChoice ch = choose_index(B, T, DI, E_cap, topk, di.num_sms);
     if (ch.bytes > (size_t)HSA_NOALLOC_SCRATCH_BYTES)
         return fail(HSA_ERR_WORKSPACE,
                     "hsa_index_topk_noalloc: these sizes need %zu bytes of scratch, the built-in scratch holds %u; "
@@ -433,6 +444,7 @@ extern "C" hsa_status_t hsa_index_topk_noalloc(const int8_t *q_idx, int64_t q_sb
     cudaError_t e = cudaMemsetAsync(ws, 0, ch.bytes, s);
     if (e != cudaSuccess) return launched(e, "index_topk_noalloc (clear scratch)");
     if (ch.fused) return launched(hsa::launch_index_fused(a, ch.fp, ws, s), "index_topk_noalloc (fused)");
+    if (ch.prefill) return launched(hsa::launch_index_prefill(a, ch.pp, ws, di.num_sms, s), "index_topk_noalloc (tensor cores)");
     for (int r0 = 0; r0 < rows; r0 += ch.group) {
         e = hsa::launch_index_topk(a, ch.tp, ws, r0, s);
         if (e != cudaSuccess) return launched(e, "index_topk_noalloc");

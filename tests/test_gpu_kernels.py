@@ -323,3 +323,16 @@ def test_attn_decode_batch_invariant(lib, dense):
     for i in range(B):
         o1, l1 = run([i])
         assert torch.equal(o1[0], full_o[i]) and torch.equal(l1[0], full_l[i])
+
+
+@pytest.mark.parametrize("DI,topk", [(64, 512), (64, 1024), (128, 256)])
+def test_index_topk_many_rows_tensor_core_path(lib, DI, topk):
+    # T >= 128 query rows per sequence and a long cache take the tensor-core path;
+    # one tile is ragged (T % 128 != 0) and rows near the start see few entries.
+    E_cap = 20000 + 37
+    _index_case(lib, B=2, T=300, E_cap=E_cap, DI=DI, m=4, topk=topk, pos0=[4 * E_cap - 300, 4 * 600], seed=DI + topk)
+
+
+def test_index_topk_many_rows_heavy_ties(lib):
+    # tied scores defeat the sampled threshold; rows fall back to the exact scan
+    _index_case(lib, B=1, T=130, E_cap=6000, DI=64, m=4, topk=256, pos0=[4 * 6000 - 130], lo=-1, hi=1, seed=21)
