@@ -11,7 +11,7 @@
 //   convert   int8 -> bf16 copies of the query and entry vectors (workspace).
 //   sample    per 128-query tile, score every 16th 128-entry tile, keep a
 //             per-row 128-bin histogram over the row's score bound and set the
-//             row's candidate threshold tau so that about 1.6*k entries of the
+//             row's candidate threshold tau so that about 2*k entries of the
 //             whole row are expected at or above it.
 //   collect   per (128-query tile, entry segment), score every entry; a row's
 //             thread appends (score, index) of the entries at or above tau, in
@@ -50,9 +50,11 @@ struct PfArgs {
     const int8_t *k8;      // original int8 entry vectors (fallback)
     int64_t k_sb, k_se;
     float *tau;            // [B*T]
-    int2 *lists;           // [B*T][S][cap_seg]
+    int32_t *lists;        // [B*T][S][list_stride] entry indices (scores are recomputed exactly later)
     int *counts;           // [B*T][S]
     int n_seg, cap_seg, seg_tiles;
+    int list_stride;  // entries between consecutive lists: cap_seg padded off a power of two, so the
+                      // lists of neighbouring rows do not all map to the same memory partition
     int32_t *idx_out, *cnt_out;
 };
 
@@ -236,20 +238,30 @@ __global__ void __launch_bounds__(kThreads, SAMPLE ? 1 : 2)
         float lo = 0.f, inv_w = 0.f;
         float tau = 0.f;
         int cnt = 0;
-        int2 *my_list = nullptr;
+        int32_t *my_list = nullptr;
         if (SAMPLE) {
             int sabs = 0;
-            if (live)
-                for (int c = 0; c < a.DI; ++c) {
-                    const int v = a.q8[b * a.q_sb + (int64_t)t * a.q_st + c];
-                    sabs += v < 0 ? -v : v;
+            if (live) {
+                const int4 *qp = reinterpret_cast<const int4 *>(a.q8 + b * a.q_sb + (int64_t)t * a.q_st);
+#pragma unroll
+                for (int c = 0; c < DI / 16; ++c) {
+                    const int4 w4 = qp[c];
+                    const int wv[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+                    for (int h = 0; h < 4; ++h)
+#pragma unroll
+                        for (int by = 0; by < 4; ++by) {
+                            const int x = (int)(int8_t)(wv[h] >> (8 * by));
+                            sabs += x < 0 ? -x : x;
+                        }
                 }
+            }
             const float R = 128.f * (float)sabs + 1.f;
             lo = -R;
             inv_w = (float)kBins / (2.f * R);
         } else {
             tau = live ? a.tau[row] : INFINITY;
-            my_list = a.lists + (row * a.n_seg + seg) * (int64_t)a.cap_seg;
+            my_list = a.lists + (row * a.n_seg + seg) * (int64_t)a.list_stride;
         }
         bool ok = true;
         for (int it = 0; it < n_my && ok; ++it) {
@@ -258,46 +270,56 @@ __global__ void __launch_bounds__(kThreads, SAMPLE ? 1 : 2)
             if (!ok) break;
             tc::fence_after();
             const int64_t j0 = (int64_t)(tile_begin + it * tile_step) * kN;
+            const int64_t rem = E - j0;
+            const int n_valid = rem <= 0 ? 0 : (rem >= kN ? kN : (int)rem);  // columns of this row that count
+            uint32_t v[kN];
 #pragma unroll
-            for (int c = 0; c < kN / 32; ++c) {
-                uint32_t v[32];
-                tc::tmem_ld32(tmem + sb * kN + lane_off + c * 32, v);
-                tc::tmem_wait_ld();
-                if (SAMPLE) {
+            for (int c = 0; c < kN / 32; ++c) tc::tmem_ld32(tmem + sb * kN + lane_off + c * 32, v + c * 32);
+            tc::tmem_wait_ld();
+            tc::fence_before();
+            arrive(&bars.s_free[sb]);  // S has been copied to registers
+            if (SAMPLE) {
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        const int64_t j = j0 + c * 32 + e;
-                        if (j < E) {
-                            int bin = (int)((__uint_as_float(v[e]) - lo) * inv_w);
-                            bin = bin < 0 ? 0 : (bin >= kBins ? kBins - 1 : bin);
-                            sHist[bin * kRows + r] += 1u;
-                        }
-                    }
-                } else {
+                for (int e = 0; e < kN; ++e) {
+                    int bin = __float2int_rz((__uint_as_float(v[e]) - lo) * inv_w);
+                    bin = bin < 0 ? 0 : (bin >= kBins ? kBins - 1 : bin);
+                    atomicAdd(&sHist[bin * kRows + r], e < n_valid ? 1u : 0u);  // no branch per element
+                }
+            } else {
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        const float sc = __uint_as_float(v[e]);
-                        const int64_t j = j0 + c * 32 + e;
-                        if (sc >= tau && j < E) {
-                            if (cnt < a.cap_seg) my_list[cnt] = make_int2((int)sc, (int)j);
+                for (int c = 0; c < kN / 32; ++c) {
+                    // most 32-column chunks hold no candidate: test their max first
+                    float mx = __uint_as_float(v[c * 32]);
+#pragma unroll
+                    for (int e = 1; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(v[c * 32 + e]));
+                    if (mx >= tau && c * 32 < n_valid) {
+                        // branch-free hit mask, then one iteration per hit (usually 0-2)
+                        uint32_t hits = 0;
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) hits |= (uint32_t)(__uint_as_float(v[c * 32 + e]) >= tau) << e;
+                        const int nv = n_valid - c * 32;
+                        if (nv < 32) hits &= (1u << nv) - 1u;
+                        while (hits) {
+                            const int e = __ffs(hits) - 1;
+                            hits &= hits - 1u;
+                            if (cnt < a.cap_seg) my_list[cnt] = (int32_t)(j0 + c * 32 + e);
                             ++cnt;
                         }
                     }
                 }
             }
-            tc::fence_before();
-            arrive(&bars.s_free[sb]);
         }
         if (!ok) s_abort = 1;
         if (live) {
             if (SAMPLE) {
-                // threshold: expect ~1.6*k of the row's E entries at or above it
+                // threshold: expect ~2*k of the row's E entries at or above it (the sample
+                // count above it is ~2*k/16, so falling short of k is a > 5 sigma event)
                 const int kE = (int)(E < a.topk ? E : a.topk);
                 int n_samp = 0;
                 for (int i = 0; i < kBins; ++i) n_samp += (int)sHist[i * kRows + r];
                 float th = -INFINITY;
                 if (E > 4 * kE && n_samp > 0) {
-                    const float want = 1.6f * (float)kE * (float)n_samp / (float)E;
+                    const float want = 2.0f * (float)kE * (float)n_samp / (float)E;
                     float cum = 0.f;
                     for (int i = kBins - 1; i >= 0; --i) {
                         cum += (float)sHist[i * kRows + r];
@@ -321,7 +343,8 @@ __global__ void __launch_bounds__(kThreads, SAMPLE ? 1 : 2)
 
 // --------------------------------------------------------------- selection
 constexpr int kSelThreads = 256;
-constexpr int kSelCap = 8192;  // candidates held in shared memory
+constexpr int kSelWarps = kSelThreads / 32;
+constexpr int kSelCap = 4096;  // candidates held in shared memory (2-3k are expected)
 
 __device__ __forceinline__ int dot16(const int4 &x, const int4 &y) {
     int s = __dp4a(x.x, y.x, 0);
@@ -330,105 +353,114 @@ __device__ __forceinline__ int dot16(const int4 &x, const int4 &y) {
     return __dp4a(x.w, y.w, s);
 }
 
-// Exact selection over candidates held in shared memory in ascending index order.
-// Keys are biased scores (>= 0).  Writes min(kE, n) indices (n >= kE required).
-__device__ void select_sorted(const uint32_t *s_u, const int32_t *s_j, int n, int kE, int key_bits, unsigned *hist,
-                              int *s_scan, int *s_misc, int32_t *out) {
+// The bin of hist[0 .. nb) (bin index grows with the key) where the count taken from
+// the top first reaches `want`: s_misc[slot] = bin, s_misc[slot + 1] = count above it.
+__device__ void find_bin(const unsigned *hist, int nb, int want, int *s_scan, int *s_misc, int slot) {
+    const int per = nb / kSelThreads, top = nb - 1 - threadIdx.x * per;
+    int local = 0;
+    for (int q = 0; q < per; ++q) local += (int)hist[top - q];
+    int tot;
+    const int before = block_exclusive_sum(local, s_scan, tot);
+    if (before < want && before + local >= want) {
+        int cum = before;
+        for (int q = 0; q < per; ++q) {
+            const int hv = (int)hist[top - q];
+            if (cum + hv >= want) {
+                s_misc[slot] = top - q;
+                s_misc[slot + 1] = cum;
+                break;
+            }
+            cum += hv;
+        }
+    }
+    __syncthreads();
+}
+
+// Exact k-th largest key over items 0 .. n-1 (n >= kE): two radix levels of 11 and
+// key_bits - 11 bits.  Returns the threshold key T and how many items equal to T
+// belong to the top kE (the rest of the top kE are the items above T).
+template <class KeyF>
+__device__ void kth_key(int64_t n, int kE, int key_bits, KeyF key, unsigned *hist, int *s_scan, int *s_misc,
+                        uint32_t &T, int &n_eq_need) {
     const int shift = key_bits - 11;
-    // level 1: 2048 bins of the top bits
     for (int i = threadIdx.x; i < 2048; i += kSelThreads) hist[i] = 0;
     __syncthreads();
-    for (int i = threadIdx.x; i < n; i += kSelThreads) atomicAdd(&hist[s_u[i] >> shift], 1u);
+    for (int64_t i = threadIdx.x; i < n; i += kSelThreads) atomicAdd(&hist[key(i) >> shift], 1u);
     __syncthreads();
-    {
-        const int per = 2048 / kSelThreads, top = 2047 - threadIdx.x * per;
-        int local = 0;
-        for (int q = 0; q < per; ++q) local += (int)hist[top - q];
-        int tot;
-        const int before = block_exclusive_sum(local, s_scan, tot);
-        if (before < kE && before + local >= kE) {
-            int cum = before;
-            for (int q = 0; q < per; ++q) {
-                const int hv = (int)hist[top - q];
-                if (cum + hv >= kE) {
-                    s_misc[0] = top - q;
-                    s_misc[1] = cum;
-                    break;
-                }
-                cum += hv;
-            }
-        }
-        __syncthreads();
-    }
+    find_bin(hist, 2048, kE, s_scan, s_misc, 0);
     const uint32_t b1 = (uint32_t)s_misc[0];
-    const int above = s_misc[1];
-    const int need = kE - above;
-    // level 2: low bits inside b1 (at most 2^11 bins for DI <= 128)
+    const int need = kE - s_misc[1];
     const int nb2 = 1 << shift;
     for (int i = threadIdx.x; i < nb2; i += kSelThreads) hist[i] = 0;
     __syncthreads();
-    for (int i = threadIdx.x; i < n; i += kSelThreads)
-        if ((s_u[i] >> shift) == b1) atomicAdd(&hist[s_u[i] & (uint32_t)(nb2 - 1)], 1u);
+    for (int64_t i = threadIdx.x; i < n; i += kSelThreads) {
+        const uint32_t u = key(i);
+        if ((u >> shift) == b1) atomicAdd(&hist[u & (uint32_t)(nb2 - 1)], 1u);
+    }
     __syncthreads();
-    {
-        const int per = nb2 / kSelThreads, top = nb2 - 1 - threadIdx.x * per;
-        int local = 0;
-        for (int q = 0; q < per; ++q) local += (int)hist[top - q];
-        int tot;
-        const int before = block_exclusive_sum(local, s_scan, tot);
-        if (before < need && before + local >= need) {
-            int cum = before;
-            for (int q = 0; q < per; ++q) {
-                const int hv = (int)hist[top - q];
-                if (cum + hv >= need) {
-                    s_misc[2] = top - q;
-                    s_misc[3] = cum;
-                    break;
-                }
-                cum += hv;
-            }
-        }
-        __syncthreads();
-    }
-    const uint32_t T = (b1 << shift) | (uint32_t)s_misc[2];
-    const int n_eq_need = need - s_misc[3];
-    // ordered compaction (candidates are in index order)
-    const int per = (n + kSelThreads - 1) / kSelThreads, my0 = threadIdx.x * per;
-    int eq = 0;
-    for (int q = 0; q < per; ++q) {
-        const int i = my0 + q;
-        if (i < n && s_u[i] == T) ++eq;
-    }
-    int tot;
-    int er = block_exclusive_sum(eq, s_scan, tot);
-    int nsel = 0;
-    {
-        int e2 = er;
-        for (int q = 0; q < per; ++q) {
-            const int i = my0 + q;
-            if (i >= n) break;
-            if (s_u[i] > T) ++nsel;
-            else if (s_u[i] == T) { nsel += e2 < n_eq_need; ++e2; }
-        }
-    }
-    int o = block_exclusive_sum(nsel, s_scan, tot);
-    for (int q = 0; q < per; ++q) {
-        const int i = my0 + q;
-        if (i >= n) break;
-        bool take = s_u[i] > T;
-        if (s_u[i] == T) { take = er < n_eq_need; ++er; }
-        if (take) out[o++] = s_j[i];
-    }
+    find_bin(hist, nb2, need, s_scan, s_misc, 2);
+    T = (b1 << shift) | (uint32_t)s_misc[2];
+    n_eq_need = need - s_misc[3];
 }
 
-__global__ void __launch_bounds__(kSelThreads) select_kernel(PfArgs a, int key_bits) {
+// Ordered compaction of items 0 .. n-1 (ascending entry index): keeps every item whose
+// key is above T and the first n_eq_need items whose key equals T, and writes their
+// entry indices to out in item order.  Each warp owns one contiguous run of items;
+// output slots come from per-warp counts and lane ballots.
+template <class KeyF, class IdxF>
+__device__ void ordered_take(int64_t n, uint32_t T, int n_eq_need, KeyF key, IdxF idx, int *s_w, int32_t *out) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t run = ((n + kSelWarps - 1) / kSelWarps + 31) & ~(int64_t)31;
+    const int64_t w0 = warp * run < n ? warp * run : n;
+    const int64_t w1 = w0 + run < n ? w0 + run : n;
+    int gt = 0, eq = 0;
+    for (int64_t i = w0 + lane; i < w1; i += 32) {
+        const uint32_t u = key(i);
+        gt += u > T;
+        eq += u == T;
+    }
+    gt = __reduce_add_sync(~0u, gt);
+    eq = __reduce_add_sync(~0u, eq);
+    if (lane == 0) {
+        s_w[warp] = gt;
+        s_w[kSelWarps + warp] = eq;
+    }
+    __syncthreads();
+    int eq_run = 0, sel_run = 0;
+    for (int v = 0; v < warp; ++v) {
+        const int ev = s_w[kSelWarps + v];
+        int tk = n_eq_need - eq_run;
+        tk = tk < 0 ? 0 : (tk > ev ? ev : tk);
+        sel_run += s_w[v] + tk;
+        eq_run += ev;
+    }
+    const uint32_t lt = (1u << lane) - 1u;
+    for (int64_t base = w0; base < w1; base += 32) {  // warp-uniform trip count
+        const int64_t i = base + lane;
+        const bool valid = i < w1;
+        const uint32_t u = valid ? key(i) : 0u;
+        const bool is_eq = valid && u == T;
+        const uint32_t em = __ballot_sync(~0u, is_eq);
+        const bool take = (valid && u > T) || (is_eq && eq_run + __popc(em & lt) < n_eq_need);
+        const uint32_t tm = __ballot_sync(~0u, take);
+        if (take) out[sel_run + __popc(tm & lt)] = idx(i);
+        eq_run += __popc(em);
+        sel_run += __popc(tm);
+    }
+    __syncthreads();
+}
+
+template <int DI>
+__global__ void __launch_bounds__(kSelThreads, 4) select_kernel(PfArgs a) {
+    constexpr int kKeyBits = DI == 64 ? 21 : 22;  // biased keys lie in [0, 2 * DI * 127^2]
     extern __shared__ __align__(16) unsigned char smem[];
-    uint32_t *s_u = reinterpret_cast<uint32_t *>(smem);         // [kSelCap]
-    int32_t *s_j = reinterpret_cast<int32_t *>(s_u + kSelCap);  // [kSelCap]
+    uint32_t *s_u = reinterpret_cast<uint32_t *>(smem);            // [kSelCap]
+    int32_t *s_j = reinterpret_cast<int32_t *>(s_u + kSelCap);     // [kSelCap]
     unsigned *hist = reinterpret_cast<unsigned *>(s_j + kSelCap);  // [2048]
     __shared__ int s_scan[33];
     __shared__ int s_misc[8];
-    __shared__ int s_off[16];
+    __shared__ int s_off[17];
+    __shared__ int s_w[2 * kSelWarps];
 
     const int64_t row = blockIdx.x;
     const int b = (int)(row / a.T), t = (int)(row - (int64_t)b * a.T);
@@ -440,123 +472,77 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(PfArgs a, int key_b
     }
     const int kE = (int)(E < a.topk ? E : a.topk);
     int32_t *out = a.idx_out + row * a.topk;
+    int4 qv[DI / 16];
+    {
+        const int4 *qp = reinterpret_cast<const int4 *>(a.q8 + b * a.q_sb + (int64_t)t * a.q_st);
+#pragma unroll
+        for (int q = 0; q < DI / 16; ++q) qv[q] = qp[q];
+    }
     for (int i = kE + threadIdx.x; i < a.topk; i += kSelThreads) out[i] = -1;
     if (threadIdx.x == 0) a.cnt_out[row] = kE;
     if (kE == 0) return;
-    const int bias = a.DI * 16256;
+    const int bias = DI * 16256;
 
-    // gather the segment lists (each in index order, segments in order)
+    // the segment lists, each in index order, concatenated in segment order
     if (threadIdx.x == 0) {
         int off = 0;
         bool fits = true;
-        for (int s = 0; s < a.n_seg; ++s) {
-            const int c = a.counts[row * a.n_seg + s];
+        for (int sg = 0; sg < a.n_seg; ++sg) {
+            const int c = a.counts[row * a.n_seg + sg];
             if (c > a.cap_seg) fits = false;
-            s_off[s] = off;
+            s_off[sg] = off;
             off += c;
         }
+        s_off[a.n_seg] = off;
         s_misc[4] = off;
-        s_misc[5] = fits && off <= kSelCap && off >= kE;
+        s_misc[5] = fits && off >= kE;  // the lists hold the whole top-k
     }
     __syncthreads();
     const int n = s_misc[4];
-    if (s_misc[5]) {
-        for (int s = 0; s < a.n_seg; ++s) {
-            const int c = a.counts[row * a.n_seg + s];
-            const int2 *lst = a.lists + (row * a.n_seg + s) * (int64_t)a.cap_seg;
-            for (int i = threadIdx.x; i < c; i += kSelThreads) {
-                const int2 v = lst[i];
-                s_u[s_off[s] + i] = (uint32_t)(v.x + bias);
-                s_j[s_off[s] + i] = v.y;
-            }
+    const bool from_lists = s_misc[5];
+    const int32_t *lists_row = a.lists + row * a.n_seg * (int64_t)a.list_stride;
+    const char *kbase = reinterpret_cast<const char *>(a.k8 + b * a.k_sb);
+    auto key_of = [&](int64_t j) {
+        const int4 *kr = reinterpret_cast<const int4 *>(kbase + j * a.k_se);
+        int sc = 0;
+#pragma unroll
+        for (int q = 0; q < DI / 16; ++q) sc += dot16(qv[q], __ldg(kr + q));  // one 16-byte load each
+        return (uint32_t)(sc + bias);
+    };
+    uint32_t T;
+    int n_eq_need;
+    if (from_lists && n <= kSelCap) {
+        // common case: stage (key, index) in shared memory -- indices first (coalesced),
+        // then the keys with several independent row reads in flight per thread
+        for (int sg = 0; sg < a.n_seg; ++sg) {
+            const int c = s_off[sg + 1] - s_off[sg];
+            const int32_t *lst = lists_row + sg * (int64_t)a.list_stride;
+            for (int i = threadIdx.x; i < c; i += kSelThreads) s_j[s_off[sg] + i] = lst[i];
         }
         __syncthreads();
-        select_sorted(s_u, s_j, n, kE, key_bits, hist, s_scan, s_misc, out);
+#pragma unroll 4
+        for (int i = threadIdx.x; i < n; i += kSelThreads) s_u[i] = key_of(s_j[i]);
+        __syncthreads();
+        auto key_s = [&](int64_t i) { return s_u[i]; };
+        auto idx_s = [&](int64_t i) { return s_j[i]; };
+        kth_key(n, kE, kKeyBits, key_s, hist, s_scan, s_misc, T, n_eq_need);
+        ordered_take(n, T, n_eq_need, key_s, idx_s, s_w, out);
         return;
     }
-    // ---- exact fallback: three dp4a passes over the row's keys
-    const int lpe = a.DI / 16;
-    const int lane_e = threadIdx.x % lpe, grp = threadIdx.x / lpe, groups = kSelThreads / lpe;
-    const int4 qv = *reinterpret_cast<const int4 *>(a.q8 + b * a.q_sb + (int64_t)t * a.q_st + lane_e * 16);
-    const char *kbase = reinterpret_cast<const char *>(a.k8 + b * a.k_sb) + lane_e * 16;
-    const int shift = key_bits - 11;
-    auto key_of = [&](int64_t j, bool valid) {
-        const int4 kv = valid ? *reinterpret_cast<const int4 *>(kbase + j * a.k_se) : make_int4(0, 0, 0, 0);
-        int s = dot16(qv, kv);
-        for (int o = 1; o < lpe; o <<= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-        return (uint32_t)(s + bias);
+    // Streaming exact selection over items 0 .. n_items-1 (index order), keys
+    // recomputed on every pass: the concatenated lists when they hold the top-k but
+    // not in shared memory, otherwise every entry of the row (a sampled threshold that
+    // came out too high, or a list overflow).
+    const int64_t n_items = from_lists ? (int64_t)n : E;
+    auto index_of = [&](int64_t i) -> int32_t {
+        if (!from_lists) return (int32_t)i;
+        int sg = 0;
+        while (sg + 1 < a.n_seg && i >= s_off[sg + 1]) ++sg;
+        return lists_row[sg * (int64_t)a.list_stride + (i - s_off[sg])];
     };
-    // pass 1: level-1 histogram
-    for (int i = threadIdx.x; i < 2048; i += kSelThreads) hist[i] = 0;
-    __syncthreads();
-    for (int64_t j0 = 0; j0 < E; j0 += groups) {
-        const int64_t j = j0 + grp;
-        const uint32_t u = key_of(j, j < E);
-        if (lane_e == 0 && j < E) atomicAdd(&hist[u >> shift], 1u);
-    }
-    __syncthreads();
-    {
-        const int per = 2048 / kSelThreads, top = 2047 - threadIdx.x * per;
-        int local = 0;
-        for (int q = 0; q < per; ++q) local += (int)hist[top - q];
-        int tot;
-        const int before = block_exclusive_sum(local, s_scan, tot);
-        if (before < kE && before + local >= kE) {
-            int cum = before;
-            for (int q = 0; q < per; ++q) {
-                const int hv = (int)hist[top - q];
-                if (cum + hv >= kE) { s_misc[0] = top - q; s_misc[1] = cum; break; }
-                cum += hv;
-            }
-        }
-        __syncthreads();
-    }
-    const uint32_t b1 = (uint32_t)s_misc[0];
-    const int need = kE - s_misc[1];
-    const int nb2 = 1 << shift;
-    // pass 2: low bits inside b1
-    for (int i = threadIdx.x; i < nb2; i += kSelThreads) hist[i] = 0;
-    __syncthreads();
-    for (int64_t j0 = 0; j0 < E; j0 += groups) {
-        const int64_t j = j0 + grp;
-        const uint32_t u = key_of(j, j < E);
-        if (lane_e == 0 && j < E && (u >> shift) == b1) atomicAdd(&hist[u & (uint32_t)(nb2 - 1)], 1u);
-    }
-    __syncthreads();
-    {
-        const int per = nb2 / kSelThreads, top = nb2 - 1 - threadIdx.x * per;
-        int local = 0;
-        for (int q = 0; q < per; ++q) local += (int)hist[top - q];
-        int tot;
-        const int before = block_exclusive_sum(local, s_scan, tot);
-        if (before < need && before + local >= need) {
-            int cum = before;
-            for (int q = 0; q < per; ++q) {
-                const int hv = (int)hist[top - q];
-                if (cum + hv >= need) { s_misc[2] = top - q; s_misc[3] = cum; break; }
-                cum += hv;
-            }
-        }
-        __syncthreads();
-    }
-    const uint32_t T = (b1 << shift) | (uint32_t)s_misc[2];
-    const int n_eq_need = need - s_misc[3];
-    // pass 3: ordered compaction, one group-tile of entries at a time
-    int eq_base = 0, pos_base = 0;
-    for (int64_t j0 = 0; j0 < E; j0 += groups) {
-        const int64_t j = j0 + grp;
-        const uint32_t u = key_of(j, j < E);
-        const bool valid = lane_e == 0 && j < E;
-        const int is_eq = valid && u == T, is_gt = valid && u > T;
-        int tot_eq;
-        const int er = eq_base + block_exclusive_sum(is_eq, s_scan, tot_eq);
-        const int take = is_gt || (is_eq && er < n_eq_need);
-        int tot_sel;
-        const int o = pos_base + block_exclusive_sum(take, s_scan, tot_sel);
-        if (take) out[o] = (int32_t)j;
-        eq_base += tot_eq;
-        pos_base += tot_sel;
-    }
+    auto key_g = [&](int64_t i) { return key_of(index_of(i)); };
+    kth_key(n_items, kE, kKeyBits, key_g, hist, s_scan, s_misc, T, n_eq_need);
+    ordered_take(n_items, T, n_eq_need, key_g, index_of, s_w, out);
 }
 
 template <int DI>
@@ -584,7 +570,7 @@ size_t al256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 PrefillIndexPlan plan_index_prefill(int B, int T, int DI, int64_t E_cap, int topk, int num_sms) {
     PrefillIndexPlan p{};
-    p.ok = (DI == 64 || DI == 128) && T >= kRows && E_cap >= 4 * kN && topk <= 2048;
+    p.ok = (DI == 64 || DI == 128) && T >= kRows && E_cap >= 4 * kN && topk <= 1024;
     if (!p.ok) return p;
     const int tiles_per_b = (T + kRows - 1) / kRows;
     p.n_qtiles = B * tiles_per_b;
@@ -607,7 +593,7 @@ PrefillIndexPlan plan_index_prefill(int B, int T, int DI, int64_t E_cap, int top
     p.off_counts = off;
     off = al256(off + (size_t)rows * p.n_seg * 4);
     p.off_lists = off;
-    off = al256(off + (size_t)rows * p.n_seg * p.cap_seg * 8);
+    off = al256(off + (size_t)rows * p.n_seg * (p.cap_seg + 40) * 4);
     p.total = off;
     return p;
 }
@@ -649,10 +635,11 @@ cudaError_t launch_index_prefill(const IndexArgs &a, const PrefillIndexPlan &p, 
     pa.k_sb = a.k_sb;
     pa.k_se = a.k_se;
     pa.tau = reinterpret_cast<float *>(w + p.off_tau);
-    pa.lists = reinterpret_cast<int2 *>(w + p.off_lists);
+    pa.lists = reinterpret_cast<int32_t *>(w + p.off_lists);
     pa.counts = reinterpret_cast<int *>(w + p.off_counts);
     pa.n_seg = p.n_seg;
     pa.cap_seg = p.cap_seg;
+    pa.list_stride = p.cap_seg + 40;
     pa.seg_tiles = p.seg_tiles;
     pa.idx_out = a.idx_out;
     pa.cnt_out = a.cnt_out;
@@ -663,12 +650,16 @@ cudaError_t launch_index_prefill(const IndexArgs &a, const PrefillIndexPlan &p, 
         if ((e = launch_score<128>(tq, tk, pa, p.n_qtiles, true, s)) != cudaSuccess) return e;
         if ((e = launch_score<128>(tq, tk, pa, p.n_qtiles * p.n_seg, false, s)) != cudaSuccess) return e;
     }
-    int key_bits = 0;
-    while ((1ll << key_bits) <= (long long)a.DI * 32640) ++key_bits;
     const size_t smem = (size_t)kSelCap * 8 + 2048 * 4;
-    static unsigned long long done = 0;
-    if ((e = smem_limit_once(select_kernel, (int)smem, done)) != cudaSuccess) return e;
-    select_kernel<<<(unsigned)rows, kSelThreads, smem, s>>>(pa, key_bits);
+    if (a.DI == 64) {
+        static unsigned long long done = 0;
+        if ((e = smem_limit_once(select_kernel<64>, (int)smem, done)) != cudaSuccess) return e;
+        select_kernel<64><<<(unsigned)rows, kSelThreads, smem, s>>>(pa);
+    } else {
+        static unsigned long long done = 0;
+        if ((e = smem_limit_once(select_kernel<128>, (int)smem, done)) != cudaSuccess) return e;
+        select_kernel<128><<<(unsigned)rows, kSelThreads, smem, s>>>(pa);
+    }
     return cudaGetLastError();
 }
 
