@@ -9,13 +9,14 @@
 // exact integer scores.
 //
 //   convert   int8 -> bf16 copies of the query and entry vectors (workspace).
-//   sample    per 128-query tile, score every 16th 128-entry tile, keep a
-//             per-row 128-bin histogram over the row's score bound and set the
-//             row's candidate threshold tau so that about 2*k entries of the
-//             whole row are expected at or above it.
-//   collect   per (128-query tile, entry segment), score every entry; a row's
-//             thread appends (score, index) of the entries at or above tau, in
-//             index order, to the row's list for that segment.
+//   sample    per 128-query tile (split over a few CTAs), score every 16th
+//             128-entry tile and add to a per-row 128-bin histogram over the
+//             row's score bound.
+//   collect   per (128-query tile, entry segment): each row's thread first sets
+//             the row's candidate threshold tau from the histogram so that about
+//             2*k entries of the whole row are expected at or above it, then
+//             scores every entry and appends the indices of those at or above
+//             tau, in index order, to the row's list for that segment.
 //   select    per row: exact top-k over the concatenated lists (two radix
 //             levels, ties by index), written in ascending index order.  A row
 //             whose lists hold fewer than k candidates or overflowed falls back
@@ -38,7 +39,9 @@ constexpr int kRows = 128;    // query rows per tile
 constexpr int kN = 128;       // entries per score tile
 constexpr int kSampleEvery = 16;
 constexpr int kBins = 128;
-constexpr int kThreads = 192;  // 4 epilogue warps, MMA warp, TMA warp
+constexpr int kHalf = kN / 2;  // entries per column half of an S tile
+constexpr int kEpiWarps = 8;   // two per TMEM lane quadrant, one per column half
+constexpr int kThreads = (kEpiWarps + 2) * 32;  // epilogue warps, MMA warp, TMA warp
 constexpr unsigned long long kWaitLimit = 1ull << 24;
 
 struct PfArgs {
@@ -49,10 +52,12 @@ struct PfArgs {
     int64_t q_sb, q_st;
     const int8_t *k8;      // original int8 entry vectors (fallback)
     int64_t k_sb, k_se;
-    float *tau;            // [B*T]
+    uint32_t *hist;        // [B*T][kBins] sampled score histogram per row (zero between calls)
+    int sample_split;      // CTAs sharing one query tile's sampled entry tiles
     int32_t *lists;        // [B*T][S][list_stride] entry indices (scores are recomputed exactly later)
     int *counts;           // [B*T][S]
     int n_seg, cap_seg, seg_tiles;
+    int n_lists;      // 2 * n_seg: lists of a row, in index order when concatenated
     int list_stride;  // entries between consecutive lists: cap_seg padded off a power of two, so the
                       // lists of neighbouring rows do not all map to the same memory partition
     int32_t *idx_out, *cnt_out;
@@ -66,6 +71,20 @@ __device__ __forceinline__ bool wait_bar(uint64_t *bar, unsigned parity, volatil
     raise_flag(FLAG_INDEX_RANGE | 0x800u);
     *abort = 1;
     return false;
+}
+constexpr uint64_t kTwo2 = 0x4000000040000000ull;   // (2.0f, 2.0f)
+constexpr uint64_t kBias2 = 0x4B0000004B000000ull;  // (2^23, 2^23)
+// Two fp32 fused multiply-adds in one packed instruction.
+__device__ __forceinline__ uint64_t fma_f32x2(uint64_t x, uint64_t y, uint64_t z) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;\n" : "=l"(d) : "l"(x), "l"(y), "l"(z));
+    return d;
+}
+// Two fp32 additions in one packed instruction (lanes: low and high 32 bits).
+__device__ __forceinline__ uint64_t add_f32x2(uint64_t x, uint64_t y) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;\n" : "=l"(d) : "l"(x), "l"(y));
+    return d;
 }
 __device__ __forceinline__ void arrive(uint64_t *bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(smem_u32(bar)) : "memory");
@@ -110,6 +129,61 @@ struct __align__(8) Bars {
     uint64_t q_full, k_full[4], k_empty[4], s_full[2], s_free[2], fin;
 };
 
+// Histogram range of one query row: every score lies within +-(128 * sum|q| + 1).
+__device__ __forceinline__ void row_bins(const int8_t *q, int DI, float &lo, float &inv_w) {
+    int sabs = 0;
+    const int4 *qp = reinterpret_cast<const int4 *>(q);
+    for (int c = 0; c < DI / 16; ++c) {
+        const int4 w4 = qp[c];
+        const int wv[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+        for (int h = 0; h < 4; ++h)
+#pragma unroll
+            for (int by = 0; by < 4; ++by) {
+                const int x = (int)(int8_t)(wv[h] >> (8 * by));
+                sabs += x < 0 ? -x : x;
+            }
+    }
+    const float R = 128.f * (float)sabs + 1.f;
+    lo = -R;
+    inv_w = (float)kBins / (2.f * R);
+}
+
+// Candidate threshold of a row from its sampled histogram: about 2*k of the row's E
+// entries are expected at or above it (the sample count above it is ~2*k/16, so the
+// row falling short of k candidates is a > 5 sigma event; select still handles it).
+// -inf (every entry a candidate) when the row has at most 4*k entries.
+__device__ float row_threshold(const uint32_t *hist, int64_t E, int topk, float lo, float inv_w) {
+    const int kE = (int)(E < topk ? E : topk);
+    if (E <= 4 * (int64_t)kE) return -INFINITY;
+    const uint4 *h4 = reinterpret_cast<const uint4 *>(hist);
+    int n_samp = 0;
+#pragma unroll 4
+    for (int i = 0; i < kBins / 4; ++i) {
+        const uint4 x = h4[i];
+        n_samp += (int)(x.x + x.y + x.z + x.w);
+    }
+    if (n_samp == 0) return -INFINITY;
+    const float want = 2.0f * (float)kE * (float)n_samp / (float)E;
+    float cum = 0.f;
+#pragma unroll 1
+    for (int i = kBins - 1; i >= 0; --i) {
+        const float c = (float)hist[i];
+        if (cum + c >= want) {
+            // the samples still wanted, taken as spread evenly over bin i
+            const float f = (want - cum) / c;
+            return floorf(lo + ((float)(i + 1) - f) / inv_w);
+        }
+        cum += c;
+    }
+    return -INFINITY;
+}
+
+// Column half h of an S tile (entries [64h, 64h + 64)) is fed from its own run of
+// 64-entry blocks.  collect: the CTA's segment is cut into two halves of whole
+// blocks and step `it` scores block `it` of each half, so each half's list comes out
+// in index order and the half-0 list precedes the half-1 list.  sample: the two
+// halves of one 128-entry tile.
 template <int DI, bool SAMPLE>
 __global__ void __launch_bounds__(kThreads, SAMPLE ? 1 : 2)
     score_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k, PfArgs a) {
@@ -123,29 +197,37 @@ __global__ void __launch_bounds__(kThreads, SAMPLE ? 1 : 2)
     __shared__ uint32_t s_tmem;
     __shared__ int s_abort;
 
-    // work item: query tile of one sequence, entry segment
+    // work item: query tile of one sequence, entry segment (sample: share of the sampled tiles)
     const int tiles_per_b = (a.T + kRows - 1) / kRows;
     const int item = blockIdx.x;
-    const int seg = SAMPLE ? 0 : item % a.n_seg;
-    const int qtile = SAMPLE ? item : item / a.n_seg;
+    const int seg = SAMPLE ? item % a.sample_split : item % a.n_seg;
+    const int qtile = SAMPLE ? item / a.sample_split : item / a.n_seg;
     const int b = qtile / tiles_per_b;
     const int t0 = (qtile - b * tiles_per_b) * kRows;
     const int64_t p_last = a.q_pos0[b] + (t0 + kRows - 1 < a.T ? t0 + kRows - 1 : a.T - 1);
     int64_t E_last = num_entries(p_last, a.m);
     if (E_last > a.E_cap) E_last = a.E_cap;
-    const int n_tiles_row = (int)((E_last + kN - 1) / kN);
-    // tiles this CTA scores: every kSampleEvery-th (sample) or its segment's range
-    int tile_begin, tile_step, n_my;
+    int n_my;                        // steps (S tiles) of this CTA
+    int64_t tile_begin = 0, tile_step = 0;  // sample: 128-entry tiles scored
+    int64_t seg_begin = 0, mid = 0, seg_end = 0;  // collect: entry ranges of the halves
     if (SAMPLE) {
-        tile_begin = 0;
-        tile_step = kSampleEvery;
-        n_my = (n_tiles_row + kSampleEvery - 1) / kSampleEvery;
+        const int64_t n_tiles_row = (E_last + kN - 1) / kN;
+        tile_begin = (int64_t)seg * kSampleEvery;
+        tile_step = (int64_t)kSampleEvery * a.sample_split;
+        n_my = n_tiles_row > tile_begin ? (int)((n_tiles_row - tile_begin + tile_step - 1) / tile_step) : 0;
     } else {
-        tile_begin = seg * a.seg_tiles;
-        tile_step = 1;
-        const int end = min(n_tiles_row, tile_begin + a.seg_tiles);
-        n_my = end > tile_begin ? end - tile_begin : 0;
+        seg_begin = (int64_t)seg * a.seg_tiles * kN;
+        seg_end = seg_begin + (int64_t)a.seg_tiles * kN;
+        const int64_t used = (E_last < seg_end ? E_last : seg_end) - seg_begin;
+        const int nblk = used > 0 ? (int)((used + kHalf - 1) / kHalf) : 0;
+        n_my = (nblk + 1) / 2;
+        mid = seg_begin + (int64_t)n_my * kHalf;
     }
+    // first entry of column half h at step it
+    auto half_start = [&](int h, int it) -> int64_t {
+        if (SAMPLE) return (tile_begin + it * tile_step) * kN + h * kHalf;
+        return (h ? mid : seg_begin) + (int64_t)it * kHalf;
+    };
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
@@ -156,7 +238,7 @@ __global__ void __launch_bounds__(kThreads, SAMPLE ? 1 : 2)
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&bars.s_full[i], 1);
-            mbar_init(&bars.s_free[i], kRows);
+            mbar_init(&bars.s_free[i], kEpiWarps * 32);
         }
         mbar_init(&bars.fin, 1);
         fence_mbar_init();
@@ -170,7 +252,7 @@ __global__ void __launch_bounds__(kThreads, SAMPLE ? 1 : 2)
     tc::fence_after();
     const uint32_t tmem = s_tmem;
 
-    if (warp == 5) {
+    if (warp == kEpiWarps + 1) {
         if (lane == 0 && n_my > 0) {
             bool ok = true;
             mbar_expect_tx(&bars.q_full, Lay::kQ);
@@ -183,12 +265,17 @@ __global__ void __launch_bounds__(kThreads, SAMPLE ? 1 : 2)
                 const int st = it % Lay::kStages;
                 if (it >= Lay::kStages) ok = wait_bar(&bars.k_empty[st], (unsigned)(((it / Lay::kStages) - 1) & 1), &s_abort);
                 if (!ok) break;
-                const int tile = tile_begin + it * tile_step;
                 mbar_expect_tx(&bars.k_full[st], Lay::kK);
                 last[st] = it / Lay::kStages;
 #pragma unroll
-                for (int kb = 0; kb < Lay::kKB; ++kb)
-                    tc::tma_load_3d(sK + st * Lay::kK + kb * kN * 128, &tm_k, kb * 64, tile * kN, b, &bars.k_full[st]);
+                for (int h = 0; h < 2; ++h) {
+                    // rows past the tensor's end are zero-filled; past the segment they are masked
+                    const int row0 = (int)half_start(h, it);
+#pragma unroll
+                    for (int kb = 0; kb < Lay::kKB; ++kb)
+                        tc::tma_load_3d(sK + st * Lay::kK + kb * kN * 128 + h * kHalf * 128, &tm_k, kb * 64, row0, b,
+                                        &bars.k_full[st]);
+                }
             }
             if (!ok) s_abort = 1;
             volatile int never = 0;
@@ -196,7 +283,7 @@ __global__ void __launch_bounds__(kThreads, SAMPLE ? 1 : 2)
             for (int st = 0; st < Lay::kStages; ++st)
                 if (last[st] >= 0) wait_bar(&bars.k_full[st], (unsigned)(last[st] & 1), &never);
         }
-    } else if (warp == 4) {
+    } else if (warp == kEpiWarps) {
         if (lane == 0 && n_my > 0) {
             constexpr uint32_t idS = tc::idesc_bf16(kRows, kN, false, false);
             bool ok = wait_bar(&bars.q_full, 0u, &s_abort);
@@ -224,9 +311,10 @@ __global__ void __launch_bounds__(kThreads, SAMPLE ? 1 : 2)
             wait_bar(&bars.fin, 0u, &never);
         }
     } else {
-        // epilogue: thread r owns query row t0 + r of sequence b
-        const int r = threadIdx.x;
-        const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+        // epilogue: warp (quadrant q, half h); thread owns query row t0 + r, columns [64h, 64h + 64)
+        const int q = warp & 3, h = warp >> 2;
+        const int r = q * 32 + lane;
+        const uint32_t lane_off = (uint32_t)(q * 32) << 16;
         const int t = t0 + r;
         const bool live = t < a.T;
         const int64_t row = (int64_t)b * a.T + (live ? t : 0);
@@ -234,34 +322,20 @@ __global__ void __launch_bounds__(kThreads, SAMPLE ? 1 : 2)
         int64_t E = num_entries(p, a.m);
         if (E > a.E_cap) E = a.E_cap;
         if (!live) E = 0;
-        // per-row bound on |score| for the sample histogram
+        // entries of this half that count: below E, and (collect) inside the half's range
+        const int64_t limit = SAMPLE ? E : ((h ? seg_end : mid) < E ? (h ? seg_end : mid) : E);
         float lo = 0.f, inv_w = 0.f;
-        float tau = 0.f;
+        if (live) row_bins(a.q8 + b * a.q_sb + (int64_t)t * a.q_st, DI, lo, inv_w);
+        uint64_t ntau2 = 0;  // (-tau, -tau) as a packed f32 pair
+        float c1 = 0.f;      // 1 - tau
         int cnt = 0;
+        const int list_id = seg * 2 + h;
         int32_t *my_list = nullptr;
-        if (SAMPLE) {
-            int sabs = 0;
-            if (live) {
-                const int4 *qp = reinterpret_cast<const int4 *>(a.q8 + b * a.q_sb + (int64_t)t * a.q_st);
-#pragma unroll
-                for (int c = 0; c < DI / 16; ++c) {
-                    const int4 w4 = qp[c];
-                    const int wv[4] = {w4.x, w4.y, w4.z, w4.w};
-#pragma unroll
-                    for (int h = 0; h < 4; ++h)
-#pragma unroll
-                        for (int by = 0; by < 4; ++by) {
-                            const int x = (int)(int8_t)(wv[h] >> (8 * by));
-                            sabs += x < 0 ? -x : x;
-                        }
-                }
-            }
-            const float R = 128.f * (float)sabs + 1.f;
-            lo = -R;
-            inv_w = (float)kBins / (2.f * R);
-        } else {
-            tau = live ? a.tau[row] : INFINITY;
-            my_list = a.lists + (row * a.n_seg + seg) * (int64_t)a.list_stride;
+        if (!SAMPLE) {
+            const float tau = live ? row_threshold(a.hist + row * kBins, E, a.topk, lo, inv_w) : INFINITY;
+            ntau2 = ((uint64_t)__float_as_uint(-tau) << 32) | __float_as_uint(-tau);
+            c1 = 1.f - tau;
+            my_list = a.lists + (row * a.n_lists + list_id) * (int64_t)a.list_stride;
         }
         bool ok = true;
         for (int it = 0; it < n_my && ok; ++it) {
@@ -269,70 +343,79 @@ __global__ void __launch_bounds__(kThreads, SAMPLE ? 1 : 2)
             ok = wait_bar(&bars.s_full[sb], (unsigned)((it >> 1) & 1), &s_abort);
             if (!ok) break;
             tc::fence_after();
-            const int64_t j0 = (int64_t)(tile_begin + it * tile_step) * kN;
-            const int64_t rem = E - j0;
-            const int n_valid = rem <= 0 ? 0 : (rem >= kN ? kN : (int)rem);  // columns of this row that count
-            uint32_t v[kN];
-#pragma unroll
-            for (int c = 0; c < kN / 32; ++c) tc::tmem_ld32(tmem + sb * kN + lane_off + c * 32, v + c * 32);
-            tc::tmem_wait_ld();
-            tc::fence_before();
-            arrive(&bars.s_free[sb]);  // S has been copied to registers
+            const int64_t j0 = half_start(h, it);
+            const int64_t rem = limit - j0;
+            const int n_valid = rem <= 0 ? 0 : (rem >= kHalf ? kHalf : (int)rem);
             if (SAMPLE) {
+                uint32_t v[kHalf];
 #pragma unroll
-                for (int e = 0; e < kN; ++e) {
+                for (int c = 0; c < kHalf / 32; ++c)
+                    tc::tmem_ld32(tmem + sb * kN + lane_off + h * kHalf + c * 32, v + c * 32);
+                tc::tmem_wait_ld();
+                tc::fence_before();
+                arrive(&bars.s_free[sb]);  // S has been copied to registers
+#pragma unroll
+                for (int e = 0; e < kHalf; ++e) {
                     int bin = __float2int_rz((__uint_as_float(v[e]) - lo) * inv_w);
                     bin = bin < 0 ? 0 : (bin >= kBins ? kBins - 1 : bin);
                     atomicAdd(&sHist[bin * kRows + r], e < n_valid ? 1u : 0u);  // no branch per element
                 }
             } else {
+                // hit masks of the two 32-column chunks (bit e: column 32c + e scored at or
+                // above tau; scores and tau are integers below 2^24, so every step below is
+                // exact).  The chunks take different routes to balance the integer and the
+                // floating-point pipes:
+                //   chunk 0: sign bits of S - tau (packed add), gathered by funnel shifts;
+                //   chunk 1: h = sat(S + 1 - tau) is 1.0 or 0.0, gathered by a packed
+                //            Horner sum m = 2m + h over columns (e, e + 16), then the two
+                //            16-bit integers are taken from the float bits (m + 2^23).
+                uint32_t v[32];
+                tc::tmem_ld32(tmem + sb * kN + lane_off + h * kHalf, v);
+                tc::tmem_wait_ld();
+                uint32_t below0 = 0;
 #pragma unroll
-                for (int c = 0; c < kN / 32; ++c) {
-                    // most 32-column chunks hold no candidate: test their max first
-                    float mx = __uint_as_float(v[c * 32]);
+                for (int e = 30; e >= 0; e -= 2) {
+                    const uint64_t d = add_f32x2(((uint64_t)v[e + 1] << 32) | v[e], ntau2);
+                    below0 = __funnelshift_l((uint32_t)(d >> 32), below0, 1);
+                    below0 = __funnelshift_l((uint32_t)d, below0, 1);
+                }
+                tc::tmem_ld32(tmem + sb * kN + lane_off + h * kHalf + 32, v);
+                tc::tmem_wait_ld();
+                tc::fence_before();
+                arrive(&bars.s_free[sb]);  // S has been copied to registers
+                uint64_t m2 = 0;
 #pragma unroll
-                    for (int e = 1; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(v[c * 32 + e]));
-                    if (mx >= tau && c * 32 < n_valid) {
-                        // branch-free hit mask, then one iteration per hit (usually 0-2)
-                        uint32_t hits = 0;
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) hits |= (uint32_t)(__uint_as_float(v[c * 32 + e]) >= tau) << e;
-                        const int nv = n_valid - c * 32;
-                        if (nv < 32) hits &= (1u << nv) - 1u;
-                        while (hits) {
-                            const int e = __ffs(hits) - 1;
-                            hits &= hits - 1u;
-                            if (cnt < a.cap_seg) my_list[cnt] = (int32_t)(j0 + c * 32 + e);
-                            ++cnt;
-                        }
-                    }
+                for (int e = 15; e >= 0; --e) {
+                    const float h_lo = __saturatef(__uint_as_float(v[e]) + c1);
+                    const float h_hi = __saturatef(__uint_as_float(v[e + 16]) + c1);
+                    m2 = fma_f32x2(m2, kTwo2, ((uint64_t)__float_as_uint(h_hi) << 32) | __float_as_uint(h_lo));
+                }
+                m2 = add_f32x2(m2, kBias2);
+                const uint32_t hits1 = __byte_perm((uint32_t)m2, (uint32_t)(m2 >> 32), 0x5410);
+                uint64_t hits = ((uint64_t)hits1 << 32) | ~below0;
+                if (n_valid < kHalf) hits &= (1ull << n_valid) - 1ull;
+                while (hits) {  // usually 0-3 per 64 columns
+                    const int e = __ffsll((long long)hits) - 1;
+                    hits &= hits - 1ull;
+                    if (cnt < a.cap_seg) my_list[cnt] = (int32_t)(j0 + e);
+                    ++cnt;
                 }
             }
         }
         if (!ok) s_abort = 1;
-        if (live) {
-            if (SAMPLE) {
-                // threshold: expect ~2*k of the row's E entries at or above it (the sample
-                // count above it is ~2*k/16, so falling short of k is a > 5 sigma event)
-                const int kE = (int)(E < a.topk ? E : a.topk);
-                int n_samp = 0;
-                for (int i = 0; i < kBins; ++i) n_samp += (int)sHist[i * kRows + r];
-                float th = -INFINITY;
-                if (E > 4 * kE && n_samp > 0) {
-                    const float want = 2.0f * (float)kE * (float)n_samp / (float)E;
-                    float cum = 0.f;
-                    for (int i = kBins - 1; i >= 0; --i) {
-                        cum += (float)sHist[i * kRows + r];
-                        if (cum >= want) {
-                            th = floorf(lo + (float)i / inv_w);
-                            break;
-                        }
-                    }
+        if (SAMPLE) {
+            // both halves have added to the row's bins (every epilogue warp reaches this
+            // barrier: the loop above is bounded), then each flushes half of the bins
+            asm volatile("bar.sync 1, %0;\n" ::"r"(kEpiWarps * 32) : "memory");
+            if (live) {
+                uint32_t *gh = a.hist + row * kBins;
+                for (int i = h * (kBins / 2); i < (h + 1) * (kBins / 2); ++i) {
+                    const uint32_t c = sHist[i * kRows + r];
+                    if (c) atomicAdd(gh + i, c);
                 }
-                a.tau[row] = th;
-            } else {
-                a.counts[row * a.n_seg + seg] = cnt;
             }
+        } else if (live) {
+            a.counts[row * a.n_lists + list_id] = cnt;
         }
     }
     tc::fence_before();
@@ -459,7 +542,7 @@ __global__ void __launch_bounds__(kSelThreads, 4) select_kernel(PfArgs a) {
     unsigned *hist = reinterpret_cast<unsigned *>(s_j + kSelCap);  // [2048]
     __shared__ int s_scan[33];
     __shared__ int s_misc[8];
-    __shared__ int s_off[17];
+    __shared__ int s_off[33];
     __shared__ int s_w[2 * kSelWarps];
 
     const int64_t row = blockIdx.x;
@@ -472,6 +555,7 @@ __global__ void __launch_bounds__(kSelThreads, 4) select_kernel(PfArgs a) {
     }
     const int kE = (int)(E < a.topk ? E : a.topk);
     int32_t *out = a.idx_out + row * a.topk;
+    for (int i = threadIdx.x; i < kBins; i += kSelThreads) a.hist[row * kBins + i] = 0;  // left zero
     int4 qv[DI / 16];
     {
         const int4 *qp = reinterpret_cast<const int4 *>(a.q8 + b * a.q_sb + (int64_t)t * a.q_st);
@@ -487,20 +571,20 @@ __global__ void __launch_bounds__(kSelThreads, 4) select_kernel(PfArgs a) {
     if (threadIdx.x == 0) {
         int off = 0;
         bool fits = true;
-        for (int sg = 0; sg < a.n_seg; ++sg) {
-            const int c = a.counts[row * a.n_seg + sg];
+        for (int sg = 0; sg < a.n_lists; ++sg) {
+            const int c = a.counts[row * a.n_lists + sg];
             if (c > a.cap_seg) fits = false;
             s_off[sg] = off;
             off += c;
         }
-        s_off[a.n_seg] = off;
+        s_off[a.n_lists] = off;
         s_misc[4] = off;
         s_misc[5] = fits && off >= kE;  // the lists hold the whole top-k
     }
     __syncthreads();
     const int n = s_misc[4];
     const bool from_lists = s_misc[5];
-    const int32_t *lists_row = a.lists + row * a.n_seg * (int64_t)a.list_stride;
+    const int32_t *lists_row = a.lists + row * a.n_lists * (int64_t)a.list_stride;
     const char *kbase = reinterpret_cast<const char *>(a.k8 + b * a.k_sb);
     auto key_of = [&](int64_t j) {
         const int4 *kr = reinterpret_cast<const int4 *>(kbase + j * a.k_se);
@@ -514,7 +598,7 @@ __global__ void __launch_bounds__(kSelThreads, 4) select_kernel(PfArgs a) {
     if (from_lists && n <= kSelCap) {
         // common case: stage (key, index) in shared memory -- indices first (coalesced),
         // then the keys with several independent row reads in flight per thread
-        for (int sg = 0; sg < a.n_seg; ++sg) {
+        for (int sg = 0; sg < a.n_lists; ++sg) {
             const int c = s_off[sg + 1] - s_off[sg];
             const int32_t *lst = lists_row + sg * (int64_t)a.list_stride;
             for (int i = threadIdx.x; i < c; i += kSelThreads) s_j[s_off[sg] + i] = lst[i];
@@ -537,7 +621,7 @@ __global__ void __launch_bounds__(kSelThreads, 4) select_kernel(PfArgs a) {
     auto index_of = [&](int64_t i) -> int32_t {
         if (!from_lists) return (int32_t)i;
         int sg = 0;
-        while (sg + 1 < a.n_seg && i >= s_off[sg + 1]) ++sg;
+        while (sg + 1 < a.n_lists && i >= s_off[sg + 1]) ++sg;
         return lists_row[sg * (int64_t)a.list_stride + (i - s_off[sg])];
     };
     auto key_g = [&](int64_t i) { return key_of(index_of(i)); };
@@ -582,18 +666,22 @@ PrefillIndexPlan plan_index_prefill(int B, int T, int DI, int64_t E_cap, int top
     p.seg_tiles = (n_tiles_row + seg - 1) / seg;
     p.n_seg = (n_tiles_row + p.seg_tiles - 1) / p.seg_tiles;
     p.cap_seg = 4096;
+    // sampled tiles of one query tile shared by several CTAs so the sample pass fills the GPU
+    p.sample_split = num_sms / p.n_qtiles;
+    if (p.sample_split < 1) p.sample_split = 1;
+    if (p.sample_split > 8) p.sample_split = 8;
     const int64_t rows = (int64_t)B * T;
     size_t off = 0;
     p.off_q16 = off;
     off = al256(off + (size_t)rows * DI * 2);
     p.off_k16 = off;
     off = al256(off + (size_t)B * E_cap * DI * 2);
-    p.off_tau = off;
-    off = al256(off + (size_t)rows * 4);
+    p.off_hist = off;
+    off = al256(off + (size_t)rows * kBins * 4);
     p.off_counts = off;
-    off = al256(off + (size_t)rows * p.n_seg * 4);
+    off = al256(off + (size_t)rows * 2 * p.n_seg * 4);
     p.off_lists = off;
-    off = al256(off + (size_t)rows * p.n_seg * (p.cap_seg + 40) * 4);
+    off = al256(off + (size_t)rows * 2 * p.n_seg * (p.cap_seg + 40) * 4);
     p.total = off;
     return p;
 }
@@ -618,7 +706,7 @@ cudaError_t launch_index_prefill(const IndexArgs &a, const PrefillIndexPlan &p, 
     {
         const uint64_t dims[3] = {(uint64_t)a.DI, (uint64_t)a.E_cap, (uint64_t)a.B};
         const uint64_t str[2] = {(uint64_t)a.DI, (uint64_t)a.E_cap * a.DI};
-        if (!make_tmap_bf16(&tk, k16, 3, dims, str, kN)) return cudaErrorInvalidValue;
+        if (!make_tmap_bf16(&tk, k16, 3, dims, str, kHalf)) return cudaErrorInvalidValue;
     }
     PfArgs pa;
     pa.B = a.B;
@@ -634,20 +722,22 @@ cudaError_t launch_index_prefill(const IndexArgs &a, const PrefillIndexPlan &p, 
     pa.k8 = a.k;
     pa.k_sb = a.k_sb;
     pa.k_se = a.k_se;
-    pa.tau = reinterpret_cast<float *>(w + p.off_tau);
+    pa.hist = reinterpret_cast<uint32_t *>(w + p.off_hist);
+    pa.sample_split = p.sample_split;
     pa.lists = reinterpret_cast<int32_t *>(w + p.off_lists);
     pa.counts = reinterpret_cast<int *>(w + p.off_counts);
     pa.n_seg = p.n_seg;
+    pa.n_lists = 2 * p.n_seg;
     pa.cap_seg = p.cap_seg;
     pa.list_stride = p.cap_seg + 40;
     pa.seg_tiles = p.seg_tiles;
     pa.idx_out = a.idx_out;
     pa.cnt_out = a.cnt_out;
     if (a.DI == 64) {
-        if ((e = launch_score<64>(tq, tk, pa, p.n_qtiles, true, s)) != cudaSuccess) return e;
+        if ((e = launch_score<64>(tq, tk, pa, p.n_qtiles * p.sample_split, true, s)) != cudaSuccess) return e;
         if ((e = launch_score<64>(tq, tk, pa, p.n_qtiles * p.n_seg, false, s)) != cudaSuccess) return e;
     } else {
-        if ((e = launch_score<128>(tq, tk, pa, p.n_qtiles, true, s)) != cudaSuccess) return e;
+        if ((e = launch_score<128>(tq, tk, pa, p.n_qtiles * p.sample_split, true, s)) != cudaSuccess) return e;
         if ((e = launch_score<128>(tq, tk, pa, p.n_qtiles * p.n_seg, false, s)) != cudaSuccess) return e;
     }
     const size_t smem = (size_t)kSelCap * 8 + 2048 * 4;

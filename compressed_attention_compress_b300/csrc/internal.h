@@ -59,8 +59,8 @@ cudaError_t launch_index_fused(const IndexArgs &a, const FusedIndexPlan &p, void
 // Many-row indexer on tcgen05 tensor cores (index_prefill_tc.cu).
 struct PrefillIndexPlan {
     bool ok;
-    int n_qtiles, n_seg, seg_tiles, cap_seg;
-    size_t off_q16, off_k16, off_tau, off_counts, off_lists, total;
+    int n_qtiles, n_seg, seg_tiles, cap_seg, sample_split;
+    size_t off_q16, off_k16, off_hist, off_counts, off_lists, total;
 };
 PrefillIndexPlan plan_index_prefill(int B, int T, int DI, int64_t E_cap, int topk, int num_sms);
 cudaError_t launch_index_prefill(const IndexArgs &a, const PrefillIndexPlan &p, void *ws, int num_sms,
