@@ -136,13 +136,17 @@ class ClockSampler:
         return d
 
 
-def load_peaks():
+def load_peaks(kind: str = "hbm_gbs"):
+    """(peak, source): the measured copy bandwidth (GB/s) or bf16 GEMM rate (TFLOP/s)
+    of this GPU model, else the earlier single-B300 measurement."""
+    fallback = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
         with open(p) as f:
             j = json.load(f)
-        return float(j["hbm_gbs"]), "measured"
-    return 6400.0, "fallback"
+        if kind in j:
+            return float(j[kind]), "measured"
+    return fallback[kind], "fallback"
 
 
 # ------------------------------------------------------------ distributed
@@ -248,26 +252,36 @@ KERNELS_PER_STEP = 3  # compress, fused indexer/top-k, cluster attention (split 
 
 
 def capture_block(bench, steps, start, events=None):
-    """One CUDA graph of `steps` consecutive steps (replica (start+i) % R) on one
-    stream.  With `events` ([step][4] external CUDA events) the graph also records
-    the time before and after each of the three calls."""
+    """One CUDA graph of `steps` consecutive steps (replica (start+i) % R).  The new
+    block's compression runs on a second stream, beside the indexer (which does not
+    read the compressed cache); attention waits for both.  With `events`
+    ([step][4] external CUDA events) the three calls run one after another on one
+    stream, with the time recorded before and after each."""
     g = torch.cuda.CUDAGraph()
     s = torch.cuda.Stream()
+    side = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
     with torch.cuda.graph(g, stream=s):
         for i in range(steps):
             r = (start + i) % bench.R
             if events is not None:
                 events[i][0].record()
-            bench.compress(r)
-            if events is not None:
+                bench.compress(r)
                 events[i][1].record()
-            bench.index(r)
-            if events is not None:
+                bench.index(r)
                 events[i][2].record()
-            bench.attn(r)
-            if events is not None:
+                bench.attn(r)
                 events[i][3].record()
+                continue
+            fork, join = torch.cuda.Event(), torch.cuda.Event()
+            fork.record(s)
+            side.wait_event(fork)
+            with torch.cuda.stream(side):
+                bench.compress(r)
+            join.record(side)
+            bench.index(r)
+            s.wait_event(join)
+            bench.attn(r)
     torch.cuda.current_stream().wait_stream(s)
     return g
 
@@ -396,6 +410,97 @@ def run_e2e(bench, args, dev):
             "ms_per_step": dt * 1e3, "steps": steps}
 
 
+# --------------------------------------------------- chunked prefill rows
+
+def prefill_flops(wl) -> float:
+    """4*H*d FLOP per (query row, attended item): QK^T and PV, multiply-add = 2 FLOP."""
+    p = np.arange(wl.N - wl.T, wl.N, dtype=np.int64)
+    E = (p + 1) // wl.m
+    sel = np.minimum(E, wl.topk) if wl.kind == "csa" else E
+    items = sel + np.minimum(wl.window, p + 1)
+    return 4.0 * wl.B * wl.H * wl.d * float(items.sum())
+
+
+def run_prefill(dev, reps: int):
+    """Chunked prefill of 8192 new tokens on a 1,048,576-token cache, one HCA and one CSA
+    layer.  Each call is timed alone with CUDA events on the launching stream, L2
+    flushed (a 256 MiB write) before every run; median of `reps` runs after 2 warm-ups."""
+    from compressed_attention_compress_b300 import _lib as L
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    peak_tc = load_peaks(kind="bf16_tflops")
+    peak_bw, _ = load_peaks()
+
+    def timed(fn):
+        ts = []
+        for i in range(reps + 2):
+            flush.fill_(i & 255)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            if i >= 2:
+                ts.append(e0.elapsed_time(e1))
+        return statistics.median(ts)
+
+    res = {}
+    for name in ("prefill_hca", "prefill_csa"):
+        wl = WORKLOADS[name]
+        B, N, H, d, m, T = wl.B, wl.N, wl.H, wl.d, wl.m, wl.T
+        E = N // m
+        g = torch.Generator(device=dev)
+        g.manual_seed(1000 * wl.wid)
+        kr = torch.randn((B, N, d), generator=g, device=dev).to(torch.bfloat16)
+        vr = torch.randn((B, N, d), generator=g, device=dev).to(torch.bfloat16)
+        q = torch.randn((B, T, H, d), generator=g, device=dev).to(torch.bfloat16)
+        w = block_weights(m, 1000 * wl.wid + 6).to(dev)
+        kc = torch.empty((B, E, d), dtype=torch.bfloat16, device=dev)
+        vc = torch.empty_like(kc)
+        zeros = torch.zeros(B, dtype=torch.int64, device=dev)
+        full = torch.full((B,), N, dtype=torch.int64, device=dev)
+        pos0 = full - T
+        L.hsa_compress(kr, vr, zeros, pos0, (N - T) // m, w, m, kc, vc)  # the cache before the chunk
+        out = torch.empty((B, T, H, d), dtype=torch.bfloat16, device=dev)
+        r = {"workload": wl.name}
+        r["compress_chunk_ms"] = timed(lambda: L.hsa_compress(kr, vr, pos0, full, T // m, w, m, kc, vc))
+        idx = cnt = None
+        if wl.kind == "csa":
+            qi = torch.randint(-127, 128, (B, T, wl.DI), generator=g, device=dev, dtype=torch.int16).to(torch.int8)
+            ki = torch.randint(-127, 128, (B, E, wl.DI), generator=g, device=dev, dtype=torch.int16).to(torch.int8)
+            idx = torch.empty((B, T, wl.topk), dtype=torch.int32, device=dev)
+            cnt = torch.empty((B, T), dtype=torch.int32, device=dev)
+            ws_i = L.workspace(L.hsa_index_topk_workspace_size(B, T, wl.DI, E, wl.topk), device=dev)
+            r["index_ms"] = timed(lambda: L.hsa_index_topk(qi, ki, pos0, m, wl.topk, idx, cnt, ws_i))
+            p = np.arange(N - T, N, dtype=np.int64)
+            macs = float(B * ((p + 1) // m).sum() * wl.DI)
+            r["index_tflops"] = 2 * macs / (r["index_ms"] * 1e-3) / 1e12
+            r["index_frac_of_bf16_peak"] = r["index_tflops"] / peak_tc[0]
+        ws_a = L.workspace(L.hsa_attn_prefill_workspace_size(torch.bfloat16, B, T, H, d, E, m,
+                                                             wl.topk if wl.kind == "csa" else 0, wl.window),
+                           device=dev)
+        r["attn_ms"] = timed(lambda: L.hsa_attn_prefill(q, kc, vc, m, idx, cnt, kr, vr, wl.window, pos0, wl.scale,
+                                                        out, ws=ws_a))
+        flop = prefill_flops(wl)
+        r["attn_tflops"] = flop / (r["attn_ms"] * 1e-3) / 1e12
+        r["attn_frac_of_bf16_peak"] = r["attn_tflops"] / peak_tc[0]
+        if wl.kind == "csa":
+            gather = float(B * T) * (wl.topk + wl.window) * 2 * d * 2
+            r["attn_gather_gbs"] = gather / (r["attn_ms"] * 1e-3) / 1e9
+            layer = r["compress_chunk_ms"] + r["index_ms"] + r["attn_ms"]
+            r["layer_ms"] = layer
+            r["layer_tflops"] = (flop + 2 * macs) / (layer * 1e-3) / 1e12
+        else:
+            r["layer_ms"] = r["compress_chunk_ms"] + r["attn_ms"]
+        r["peak_bf16_tflops"] = peak_tc[0]
+        r["peak_source"] = peak_tc[1]
+        res[name] = {k: (round(v, 4) if isinstance(v, float) else v) for k, v in r.items()}
+        del kr, vr, q, kc, vc, out
+        torch.cuda.empty_cache()
+    return res
+
+
 # ------------------------------------------------------ oracle (CPU) arm
 
 def oracle_sample_setup(seconds_hint=True):
@@ -486,11 +591,16 @@ def main():
     ap.add_argument("--ref-budget", type=float, default=120.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--traffic", type=float, default=None, help="ncu dram bytes per index_topk launch, if known")
+    ap.add_argument("--no-prefill", action="store_true", help="skip the chunked-prefill rows")
+    ap.add_argument("--prefill-reps", type=int, default=10)
+    ap.add_argument("--prefill-only", action="store_true",
+                    help="only the chunked-prefill rows (for profiling their kernels)")
     ap.add_argument("--profile", action="store_true",
                     help="small run for ncu captures: 2 replicas, no end-to-end or CPU legs")
     args = ap.parse_args()
     if args.profile:
         args.replicas, args.block, args.no_cpu_baseline = 2, max(1, min(args.block, args.steps)), True
+        args.no_prefill = True
     # the oracle's host threads are started before any GPU work
     ws, rank, local = dist_setup(args)
     if args.impl == "reference":
@@ -498,11 +608,19 @@ def main():
         if res is not None:
             print(json.dumps(res), flush=True)
         return
+    if args.prefill_only:
+        torch.cuda.set_device(local)
+        res = run_prefill(torch.device("cuda", local), args.prefill_reps)
+        if rank == 0:
+            print(json.dumps({"prefill": res}), flush=True)
+        return
     res, bench = run_hsa(args, ws, rank, local)
+    del bench
+    torch.cuda.empty_cache()
+    if not args.no_prefill:
+        res["prefill"] = run_prefill(torch.device("cuda", local), args.prefill_reps)
     if rank == 0:
         if not args.no_cpu_baseline and ws == 1:
-            del bench
-            torch.cuda.empty_cache()
             res["cpu_baseline"] = cpu_baseline(args.cpu_budget)
         print(json.dumps(res), flush=True)
     if ws > 1:
