@@ -39,6 +39,30 @@ sys.path.insert(0, ROOT)
 from compressed_attention_compress_b300.inputs import WORKLOADS, block_weights  # noqa: E402
 
 WL = WORKLOADS["pro_csa_decode"]
+
+# DRAM bytes (read + write) of one index_fused_kernel launch on this workload, from the
+# ncu capture summarised in profiles/index_fused_kernel_pro_csa_1M_B4.md; reported only
+# while the kernel's sources are the ones that capture ran.
+INDEX_TRAFFIC = {
+    "bytes": 67210240 + 216320,
+    "sources": {
+        "compressed_attention_compress_b300/csrc/index_fused.cu":
+            "28f7a328141842f9f3275299914034562505ac39713cf05675294f3c4d73ceb5",
+        "compressed_attention_compress_b300/csrc/common.cuh":
+            "35428b34db55a12ea4c19016f4b5a1d3dbe35eca7162b0449b366e789980467b",
+        "compressed_attention_compress_b300/csrc/block_scan.cuh":
+            "ac0c74255584e15eaea3aa69860c5b08cd4267e432e4e9db82d6c3de8245161a",
+    },
+}
+
+
+def index_traffic():
+    import hashlib
+    for rel, want in INDEX_TRAFFIC["sources"].items():
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            if hashlib.sha256(f.read()).hexdigest() != want:
+                return None
+    return INDEX_TRAFFIC["bytes"]
 METRIC = "decode queries/s at 1M ctx (V4-Pro-shaped CSA layer, B=4)"
 UNIT = "queries/s"
 
@@ -363,7 +387,8 @@ def run_hsa(args, ws, rank, local):
         ach = bytes_["index_topk"] / (op_ms["index_topk"] * 1e-3) / 1e9
         out["roofline"] = {"kernel": "index_fused_kernel (hsa_index_topk; one launch per step)", "bound": "hbm",
                            "achieved": ach, "peak": peak, "unit": "GB/s", "frac": ach / peak,
-                           "traffic": args.traffic, "peak_source": peak_kind,
+                           "traffic": args.traffic if args.traffic is not None else index_traffic(),
+                           "peak_source": peak_kind,
                            "algorithmic_bytes_per_launch": bytes_["index_topk"]}
         step_ach = bytes_["step"] / (ms_step * 1e-3) / 1e9
         out["step_roofline"] = {"bound": "hbm", "achieved": step_ach, "peak": peak, "unit": "GB/s",
