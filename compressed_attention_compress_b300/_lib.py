@@ -24,7 +24,8 @@ _STATUS = {0: "HSA_OK", 1: "HSA_ERR_INVALID_ARG", 2: "HSA_ERR_UNSUPPORTED", 3: "
 # every symbol include/hsa.h declares
 EXPORTS = ["hsa_last_error", "hsa_version", "hsa_check", "hsa_compress", "hsa_index_topk_workspace_size",
            "hsa_index_topk", "hsa_index_topk_noalloc", "hsa_attn_decode_workspace_size", "hsa_attn_decode",
-           "hsa_attn_prefill_workspace_size", "hsa_attn_prefill"]
+           "hsa_attn_prefill_workspace_size", "hsa_attn_prefill", "hsa_index_scores", "hsa_topk_merge",
+           "hsa_lse_merge"]
 NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
@@ -62,6 +63,12 @@ def _load():
     lib.hsa_attn_prefill.restype = I
     lib.hsa_attn_prefill.argtypes = [P, I, I, I, I, I, P, P, I64, I64, I64, I, P, P, I, P, P, I64, I64, I64, I, P,
                                      F, P, P, P, SZ, P]
+    lib.hsa_index_scores.restype = I
+    lib.hsa_index_scores.argtypes = [P, I64, I64, P, I64, I64, I64, I, I, I, P, P, I, P, P]
+    lib.hsa_topk_merge.restype = I
+    lib.hsa_topk_merge.argtypes = [P, P, I, I, I, P, P, P]
+    lib.hsa_lse_merge.restype = I
+    lib.hsa_lse_merge.argtypes = [P, P, I, I, I, I, I, P, P, P]
     return lib
 
 
@@ -164,6 +171,29 @@ def hsa_attn_prefill(q, kc, vc, m, idx, cnt, k_raw, v_raw, window, q_pos0, scale
                               k_raw.stride(1), k_raw.shape[1], int(window), _p(q_pos0), float(scale), _p(out),
                               _p(lse), _p(ws), ws.numel() * ws.element_size() if ws is not None else 0,
                               _stream(stream)))
+
+
+def hsa_index_scores(q_idx, k_idx, idx, cnt, scores, stream=None):
+    """q_idx int8 [B, T, DI]; k_idx int8 [B, E_cap, DI]; idx int32 [B, T, topk]; cnt int32 [B, T] or None;
+    scores int32 [B, T, topk] (INT32_MIN for empty slots)."""
+    B, T, DI = q_idx.shape
+    _chk(lib.hsa_index_scores(_p(q_idx), q_idx.stride(0), q_idx.stride(1), _p(k_idx), k_idx.stride(0),
+                              k_idx.stride(1), k_idx.shape[1], B, T, DI, _p(idx), _p(cnt), idx.shape[-1], _p(scores),
+                              _stream(stream)))
+
+
+def hsa_topk_merge(scores, idx, topk, idx_out, cnt_out, stream=None):
+    """scores, idx int32 [rows, n] (idx < 0 empty; non-empty indices ascending per row);
+    idx_out int32 [rows, topk]; cnt_out int32 [rows]."""
+    rows, n = idx.shape
+    _chk(lib.hsa_topk_merge(_p(scores), _p(idx), rows, n, int(topk), _p(idx_out), _p(cnt_out), _stream(stream)))
+
+
+def hsa_lse_merge(parts_o, parts_lse, out, lse_out=None, stream=None):
+    """parts_o [S, rows, H, d]; parts_lse fp32 [S, rows, H]; out [rows, H, d]; lse_out fp32 [rows, H]."""
+    S, rows, H, d = parts_o.shape
+    _chk(lib.hsa_lse_merge(_p(parts_o), _p(parts_lse), _dt(parts_o), S, rows, H, d, _p(out), _p(lse_out),
+                           _stream(stream)))
 
 
 def workspace(nbytes: int, device="cuda"):

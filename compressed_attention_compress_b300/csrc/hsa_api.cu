@@ -451,3 +451,58 @@ extern "C" hsa_status_t hsa_index_topk_noalloc(const int8_t *q_idx, int64_t q_sb
     }
     return ok();
 }
+
+extern "C" {
+
+hsa_status_t hsa_index_scores(const int8_t *q_idx, int64_t q_sb, int64_t q_st, const int8_t *k_idx, int64_t k_sb,
+                              int64_t k_se, int64_t E_cap, int B, int T, int DI, const int32_t *idx, const int32_t *cnt,
+                              int topk, int32_t *scores, hsa_stream_t stream) {
+    if (B < 0 || T < 0 || E_cap < 0 || topk <= 0 || topk > 4096) return fail(HSA_ERR_INVALID_ARG, "bad size");
+    if (DI != 16 && DI != 32 && DI != 64 && DI != 128)
+        return fail(HSA_ERR_UNSUPPORTED, "indexer dim must be 16, 32, 64 or 128, got %d", DI);
+    if (B * (int64_t)T == 0) return ok();
+    if (!q_idx || !k_idx || !idx || !scores) return fail(HSA_ERR_INVALID_ARG, "null pointer");
+    if (!aligned16(q_idx) || !aligned16(k_idx) || q_sb % 16 || q_st % 16 || k_sb % 16 || k_se % 16)
+        return fail(HSA_ERR_UNSUPPORTED, "indexer tensors and strides must be 16-byte aligned");
+    if (k_se < DI || q_st < DI) return fail(HSA_ERR_INVALID_ARG, "indexer strides overlap rows");
+    if (B * (int64_t)T > 65535) return fail(HSA_ERR_UNSUPPORTED, "more than 65535 query rows");
+    DevInfo di;
+    hsa_status_t st = device_info(di);
+    if (st != HSA_OK) return st;
+    if ((st = pending_error()) != HSA_OK) return st;
+    hsa::IndexScoreArgs a{q_idx, q_sb, q_st, k_idx, k_sb, k_se, E_cap, B, T, DI, idx, cnt, topk, scores};
+    return launched(hsa::launch_index_scores(a, reinterpret_cast<cudaStream_t>(stream)), "index_scores");
+}
+
+hsa_status_t hsa_topk_merge(const int32_t *scores, const int32_t *idx, int rows, int n, int topk, int32_t *idx_out,
+                            int32_t *cnt_out, hsa_stream_t stream) {
+    if (rows < 0 || n <= 0 || n > (1 << 20) || topk <= 0 || topk > 4096)
+        return fail(HSA_ERR_INVALID_ARG, "bad size (rows=%d n=%d topk=%d)", rows, n, topk);
+    if (rows == 0) return ok();
+    if (!scores || !idx || !idx_out || !cnt_out) return fail(HSA_ERR_INVALID_ARG, "null pointer");
+    DevInfo di;
+    hsa_status_t st = device_info(di);
+    if (st != HSA_OK) return st;
+    if ((st = pending_error()) != HSA_OK) return st;
+    hsa::TopkMergeArgs a{scores, idx, rows, n, topk, idx_out, cnt_out};
+    return launched(hsa::launch_topk_merge(a, reinterpret_cast<cudaStream_t>(stream)), "topk_merge");
+}
+
+hsa_status_t hsa_lse_merge(const void *parts_o, const float *parts_lse, hsa_dtype_t dt, int S, int rows, int H, int d,
+                           void *out, float *lse_out, hsa_stream_t stream) {
+    if (!dtype_ok(dt)) return fail(HSA_ERR_UNSUPPORTED, "dtype %d", (int)dt);
+    if (S <= 0 || rows < 0 || H <= 0 || d <= 0 || d > 1024) return fail(HSA_ERR_INVALID_ARG, "bad size");
+    if (d % (dt == HSA_BF16 ? 8 : 4)) return fail(HSA_ERR_UNSUPPORTED, "d must be a multiple of 8 (bf16) or 4 (fp32)");
+    if (rows == 0) return ok();
+    if (rows > 65535) return fail(HSA_ERR_UNSUPPORTED, "more than 65535 rows");
+    if (!parts_o || !parts_lse || !out) return fail(HSA_ERR_INVALID_ARG, "null pointer");
+    if (!aligned16(parts_o) || !aligned16(out)) return fail(HSA_ERR_UNSUPPORTED, "parts_o and out must be 16-byte aligned");
+    DevInfo di;
+    hsa_status_t st = device_info(di);
+    if (st != HSA_OK) return st;
+    if ((st = pending_error()) != HSA_OK) return st;
+    hsa::LseMergeArgs a{parts_o, parts_lse, S, rows, H, d, out, lse_out};
+    return launched(hsa::launch_lse_merge(a, dt == HSA_BF16, reinterpret_cast<cudaStream_t>(stream)), "lse_merge");
+}
+
+}  // extern "C"

@@ -66,6 +66,34 @@ PrefillIndexPlan plan_index_prefill(int B, int T, int DI, int64_t E_cap, int top
 cudaError_t launch_index_prefill(const IndexArgs &a, const PrefillIndexPlan &p, void *ws, int num_sms,
                                  cudaStream_t s);
 
+// ------------------------------------------- context-parallel exchange (cp_merge.cu)
+struct IndexScoreArgs {
+    const int8_t *q;
+    int64_t q_sb, q_st;
+    const int8_t *k;
+    int64_t k_sb, k_se, E_cap;
+    int B, T, DI;
+    const int32_t *idx;  // [B*T, topk]
+    const int32_t *cnt;  // [B*T] or null
+    int topk;
+    int32_t *scores;     // [B*T, topk]
+};
+cudaError_t launch_index_scores(const IndexScoreArgs &a, cudaStream_t s);
+struct TopkMergeArgs {
+    const int32_t *scores, *idx;  // [rows, n]; idx < 0 marks an empty slot
+    int rows, n, topk;
+    int32_t *idx_out, *cnt_out;   // [rows, topk], [rows]
+};
+cudaError_t launch_topk_merge(const TopkMergeArgs &a, cudaStream_t s);
+struct LseMergeArgs {
+    const void *parts_o;      // [S, rows, H, d]
+    const float *parts_lse;   // [S, rows, H]
+    int S, rows, H, d;
+    void *out;                // [rows, H, d]
+    float *lse_out;           // [rows, H] or null
+};
+cudaError_t launch_lse_merge(const LseMergeArgs &a, bool bf16, cudaStream_t s);
+
 // -------------------------------------------------------------- attention
 struct AttnArgs {
     const void *q;      // [rows, H, d]

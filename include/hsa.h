@@ -225,6 +225,57 @@ HSA_API hsa_status_t hsa_attn_prefill(const void *q, hsa_dtype_t dt, int B, int 
                               void *out, float *lse, void *ws, size_t ws_bytes,
                               hsa_stream_t stream);
 
+/*
+ * Context-parallel exchange of one long sequence (no counterpart in the pages:
+ * the pages describe one GPU's attention; these three calls let several ranks
+ * that each hold a contiguous range of a sequence's compressed entries produce
+ * the same result).  Per decode step each rank runs hsa_index_topk on its own
+ * range, ships its local top-k as (score, global index) pairs, every rank
+ * merges the gathered pairs with hsa_topk_merge (the global top-k is the
+ * top-k of the union of the local top-k lists), attends to the selected
+ * entries it holds (the rank holding the newest raw tokens adds the window),
+ * and the ranks' partial (out, lse) are combined with hsa_lse_merge.
+ *
+ * hsa_index_scores -- exact indexer scores of listed entries (the score of
+ * hsa_index_topk: s_j = sum_c q_idx[b, t, c] * k_idx[b, j, c], int32).
+ *   idx        int32 [B, T, topk] entry indices (local to k_idx); slots with
+ *              j < 0 or at or beyond cnt[b, t] get INT32_MIN
+ *   cnt        int32 [B, T] or NULL (all topk slots)
+ *   scores     int32 [B, T, topk] contiguous
+ * Other arguments as hsa_index_topk.  j >= E_cap raises the device flag.
+ */
+HSA_API hsa_status_t hsa_index_scores(const int8_t *q_idx, int64_t q_sb, int64_t q_st,
+                                      const int8_t *k_idx, int64_t k_sb, int64_t k_se, int64_t E_cap,
+                                      int B, int T, int DI, const int32_t *idx, const int32_t *cnt, int topk,
+                                      int32_t *scores, hsa_stream_t stream);
+
+/*
+ * hsa_topk_merge -- exact top-k over explicit (score, index) pairs.
+ *   scores, idx  int32 [rows, n] contiguous; idx < 0 marks an empty slot.
+ *                The non-empty indices of a row must be distinct and in
+ *                ascending order (the rank-major concatenation of per-rank
+ *                ascending lists over increasing entry ranges is).
+ *   idx_out      int32 [rows, topk]: the first min(topk, non-empty) indices
+ *                under (score desc, index asc), in ascending index order,
+ *                padded with -1;  cnt_out int32 [rows] their count.
+ * 1 <= n <= 1 << 20, 1 <= topk <= 4096.
+ */
+HSA_API hsa_status_t hsa_topk_merge(const int32_t *scores, const int32_t *idx, int rows, int n, int topk,
+                                    int32_t *idx_out, int32_t *cnt_out, hsa_stream_t stream);
+
+/*
+ * hsa_lse_merge -- combine S partial attention results of the same queries
+ * over disjoint item sets: lse = ln sum_s exp(lse_s) and
+ * out = sum_s exp(lse_s - lse) * out_s (a part with lse_s = -inf is empty and
+ * weighs 0; all parts empty give out = 0, lse = -inf).
+ *   parts_o    [S, rows, H, d] of `dt`, contiguous
+ *   parts_lse  fp32 [S, rows, H], contiguous
+ *   out        [rows, H, d] of `dt`;  lse_out fp32 [rows, H] or NULL
+ * d a multiple of 4 (fp32) or 8 (bf16), d <= 1024; S >= 1.
+ */
+HSA_API hsa_status_t hsa_lse_merge(const void *parts_o, const float *parts_lse, hsa_dtype_t dt, int S, int rows,
+                                   int H, int d, void *out, float *lse_out, hsa_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

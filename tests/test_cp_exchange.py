@@ -1,0 +1,103 @@
+"""Context-parallel exchange of one long sequence (entry sharding across ranks):
+the protocol of cp.cp_decode_step run by 2 gloo ranks in separate processes and
+by 3-4 ranks emulated as threads, with the per-rank steps computed by the oracle,
+against the single-process oracle of the same decode step."""
+import os
+import socket
+
+import numpy as np
+import pytest
+import torch
+import torch.multiprocessing as mp
+
+import oracle
+from compressed_attention_compress_b300 import cp
+from tests.cp_testlib import OracleOps, ThreadGroup, cp_case, full_reference
+
+M, H, D, DI, TOPK, W = 4, 4, 16, 32, 8, 8
+SCALE = 1.0 / np.sqrt(D)
+
+
+def _shard(x, world, rank, E_cap, window_rank):
+    e0, e1 = cp.shard_bounds(E_cap, world, rank)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a))
+    return cp.Shard(rank=rank, world=world, e0=e0, kc=t(x["kc"][:, e0:e1]), vc=t(x["vc"][:, e0:e1]),
+                    k_idx=t(x["k_idx"][:, e0:e1]), k_raw=t(x["k_raw"]), v_raw=t(x["v_raw"]), window_rank=window_rank)
+
+
+def _run_rank(rank, world, x, E_cap, ctx, allgather, window_rank):
+    sh = _shard(x, world, rank, E_cap, window_rank)
+    ops = OracleOps(sh.e0, E_cap)
+    return cp.cp_decode_step(sh, torch.from_numpy(x["q"]), torch.from_numpy(x["q_idx"]),
+                             torch.tensor(ctx, dtype=torch.int64), m=M, topk=TOPK, window=W, scale=SCALE,
+                             allgather=allgather, ops=ops)
+
+
+def _check(res, x, ctx):
+    ref_idx, ref_o, ref_l = full_reference(x, ctx, M, TOPK, W, SCALE)
+    for out, lse, sel in res:
+        assert np.array_equal(sel.numpy(), ref_idx), (sel, ref_idx)
+        np.testing.assert_allclose(out.numpy(), ref_o, atol=1e-10, rtol=0)
+        np.testing.assert_allclose(lse.numpy(), ref_l, atol=1e-10, rtol=0)
+
+
+CASES = [
+    # (seed, B, E_cap, ctx_len per sequence, ties)
+    (11, 2, 64, [256, 256], False),       # every entry visible
+    (12, 2, 64, [81, 256], False),        # sequence 0: rank 1's entries are not visible yet
+    (13, 3, 64, [256, 130, 7], True),     # heavy ties (3 distinct indexer values); a sequence with one entry
+]
+
+
+def _gloo_worker(rank, world, port, case):
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    import torch.distributed as dist
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        oracle.build()
+        seed, B, E_cap, ctx, ties = case
+        x = cp_case(seed, B, E_cap, M, H, D, DI, ties)
+        res = _run_rank(rank, world, x, E_cap, ctx, cp.torch_allgather(), window_rank=world - 1)
+        _check([res], x, ctx)
+    finally:
+        dist.destroy_process_group()
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+@pytest.mark.parametrize("case", CASES, ids=["full", "short", "ties"])
+def test_cp_gloo_two_ranks(case):
+    oracle.build()
+    mp.spawn(_gloo_worker, args=(2, _free_port(), case), nprocs=2, join=True)
+
+
+@pytest.mark.parametrize("world", [1, 3, 4])
+@pytest.mark.parametrize("case", CASES, ids=["full", "short", "ties"])
+def test_cp_thread_ranks(case, world):
+    oracle.build()
+    seed, B, E_cap, ctx, ties = case
+    x = cp_case(seed, B, E_cap, M, H, D, DI, ties)
+    tg = ThreadGroup(world)
+    res = tg.run(lambda r, ag: _run_rank(r, world, x, E_cap, ctx, ag, window_rank=0))
+    _check(res, x, ctx)
+
+
+def test_cp_union_of_local_topk_is_global_topk():
+    """The property the exchange rests on, by brute force: for random shardings the
+    top-k of the union of the shards' top-k lists equals the global top-k."""
+    g = np.random.default_rng(5)
+    for _ in range(200):
+        n, k = int(g.integers(1, 60)), int(g.integers(1, 12))
+        s = g.integers(-5, 6, n)                       # many ties
+        cuts = np.sort(g.integers(0, n + 1, int(g.integers(0, 4))))
+        bounds = [0, *cuts.tolist(), n]
+        order = lambda ids: sorted(ids, key=lambda j: (-s[j], j))
+        union = []
+        for a, b in zip(bounds[:-1], bounds[1:]):
+            union += order(range(a, b))[:k]
+        assert sorted(order(union)[:k]) == sorted(order(range(n))[:k])
