@@ -310,6 +310,33 @@ def capture_block(bench, steps, start, events=None):
     return g
 
 
+def time_state_append(bench, steps: int = 64, reps: int = 20) -> float:
+    """ms per call of the state-cache form of the step's compression (hsa_compress_append:
+    one new token per sequence, completing its block), in a CUDA graph of `steps` calls."""
+    wl, L = bench.wl, bench.L
+    B, N, d = wl.B, wl.N, wl.d
+    st_k = torch.zeros((B, d), dtype=torch.float32, device=bench.dev)
+    st_v = torch.zeros_like(st_k)
+    kn, vn = bench.k_raw[:, N - 1:N], bench.v_raw[:, N - 1:N]
+    pos = bench.ctx - 1
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.graph(g, stream=s):
+        for _ in range(steps):
+            L.hsa_compress_append(kn, vn, pos, bench.w, wl.m, st_k, st_v, bench.kc, bench.vc)
+    torch.cuda.current_stream().wait_stream(s)
+    g.replay()
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for _ in range(reps):
+        g.replay()
+    t1.record()
+    torch.cuda.synchronize()
+    return t0.elapsed_time(t1) / (reps * steps)
+
+
 def run_hsa(args, ws, rank, local):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
@@ -362,6 +389,7 @@ def run_hsa(args, ws, rank, local):
             per_op["index_topk"].append(ev[i][1].elapsed_time(ev[i][2]))
             per_op["attn_decode"].append(ev[i][2].elapsed_time(ev[i][3]))
     op_ms = {k: statistics.fmean(v) for k, v in per_op.items()}
+    op_ms["compress_append"] = time_state_append(bench)
 
     cnt_total = int(sum(int(c.sum()) for c in bench.cnt[:1]))
     bytes_ = algorithmic_bytes(WL, cnt_total)

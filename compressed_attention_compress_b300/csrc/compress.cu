@@ -115,4 +115,90 @@ cudaError_t launch_compress(const CompressArgs &a, bool bf16, int num_sms, cudaS
     return cudaGetLastError();
 }
 
+// ------------------------------------------------------- state-cache append
+// Decode-time compression with a partial-block state (the incremental form of the
+// same fold): for each new token at position p, r = p mod m, the running fp32 sum
+// of the current block is reset at r = 0 and takes fmaf(w[r], x, sum) -- the same
+// operations in the same order as compress_kernel -- and at r = m - 1 the block's
+// entry p / m is rounded and written.  The raw tokens of earlier blocks are never
+// read again, so the raw cache only has to keep the attention window.
+template <typename T>
+__global__ void __launch_bounds__(128) compress_append_kernel(CompressAppendArgs a) {
+    constexpr int V = ElemTraits<T>::kVec;
+    const int nvec = a.d / V;
+    const int item = blockIdx.x * blockDim.x + threadIdx.x;
+    if (item >= a.B * nvec) return;
+    const int b = item / nvec, c = item - b * nvec;
+    const bool is_v = blockIdx.y == 1;
+    const T *x = static_cast<const T *>(is_v ? a.v_new : a.k_new) + b * a.new_sb + c * V;
+    float *st = (is_v ? a.state_v : a.state_k) + b * a.state_sb + c * V;
+    T *out = static_cast<T *>(is_v ? a.vc : a.kc) + b * a.out_sb + c * V;
+    const int64_t p0 = a.pos0[b];
+    if (p0 < 0) {
+        raise_flag(FLAG_COMPRESS_RANGE);
+        return;
+    }
+    float acc[V];
+    {
+        const float4 s0 = *reinterpret_cast<const float4 *>(st);
+        acc[0] = s0.x; acc[1] = s0.y; acc[2] = s0.z; acc[3] = s0.w;
+        if constexpr (V == 8) {
+            const float4 s1 = *reinterpret_cast<const float4 *>(st + 4);
+            acc[4] = s1.x; acc[5] = s1.y; acc[6] = s1.z; acc[7] = s1.w;
+        }
+    }
+    for (int t = 0; t < a.T; ++t) {
+        const int64_t p = p0 + t;
+        const int r = (int)(p % a.m);
+        const float wr = a.w[r];
+        const int4 xv = ld_nc_v4(x + (int64_t)t * a.new_st);
+        const uint32_t *xp = reinterpret_cast<const uint32_t *>(&xv);
+        if (r == 0) {
+#pragma unroll
+            for (int e = 0; e < V; ++e) acc[e] = 0.f;
+        }
+        if constexpr (V == 8) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                acc[2 * e] = fmaf(wr, bf16_lo(xp[e]), acc[2 * e]);
+                acc[2 * e + 1] = fmaf(wr, bf16_hi(xp[e]), acc[2 * e + 1]);
+            }
+        } else {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[e] = fmaf(wr, __uint_as_float(xp[e]), acc[e]);
+        }
+        if (r == a.m - 1) {
+            const int64_t j = p / a.m;
+            if (j >= a.E_cap) {
+                raise_flag(FLAG_COMPRESS_RANGE);
+                continue;
+            }
+            int4 o;
+            uint32_t *op = reinterpret_cast<uint32_t *>(&o);
+            if constexpr (V == 8) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) op[e] = pack_bf16x2(acc[2 * e], acc[2 * e + 1]);
+            } else {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) op[e] = __float_as_uint(acc[e]);
+            }
+            *reinterpret_cast<int4 *>(out + j * a.out_se) = o;
+        }
+    }
+    *reinterpret_cast<float4 *>(st) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    if constexpr (V == 8) *reinterpret_cast<float4 *>(st + 4) = make_float4(acc[4], acc[5], acc[6], acc[7]);
+}
+
+cudaError_t launch_compress_append(const CompressAppendArgs &a, bool bf16, cudaStream_t s) {
+    const int V = bf16 ? 8 : 4;
+    const int items = a.B * (a.d / V);
+    if (items <= 0 || a.T <= 0) return cudaSuccess;
+    dim3 grid((items + 127) / 128, 2);
+    if (bf16)
+        compress_append_kernel<__nv_bfloat16><<<grid, 128, 0, s>>>(a);
+    else
+        compress_append_kernel<float><<<grid, 128, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
 }  // namespace hsa

@@ -194,6 +194,34 @@ hsa_status_t hsa_compress(const void *k, const void *v, hsa_dtype_t dt, int B, i
                     "compress");
 }
 
+hsa_status_t hsa_compress_append(const void *k_new, const void *v_new, hsa_dtype_t dt, int B, int T, int d,
+                                 int64_t new_sb, int64_t new_st, const int64_t *pos0, const float *w, int m,
+                                 float *state_k, float *state_v, int64_t state_sb, void *kc, void *vc, int64_t out_sb,
+                                 int64_t out_se, int64_t E_cap, hsa_stream_t stream) {
+    if (!dtype_ok(dt)) return fail(HSA_ERR_UNSUPPORTED, "dtype %d", (int)dt);
+    if (B < 0 || T < 0 || d <= 0 || m <= 0 || E_cap < 0) return fail(HSA_ERR_INVALID_ARG, "bad size");
+    if (m > 4096) return fail(HSA_ERR_UNSUPPORTED, "m > 4096");
+    if (B == 0 || T == 0) return ok();
+    if (!k_new || !v_new || !pos0 || !w || !state_k || !state_v || !kc || !vc)
+        return fail(HSA_ERR_INVALID_ARG, "null pointer");
+    const int64_t vec = 16 / (int64_t)esize(dt);
+    if (d % vec || d > 512) return fail(HSA_ERR_UNSUPPORTED, "d must be a multiple of %lld and <= 512", (long long)vec);
+    if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(kc) || !aligned16(vc) || !aligned16(state_k) ||
+        !aligned16(state_v))
+        return fail(HSA_ERR_UNSUPPORTED, "tensors must be 16-byte aligned");
+    if (new_sb % vec || new_st % vec || out_sb % vec || out_se % vec || state_sb % 4)
+        return fail(HSA_ERR_UNSUPPORTED, "strides must be multiples of 16 bytes");
+    if (new_st < d || out_se < d || state_sb < d) return fail(HSA_ERR_INVALID_ARG, "row strides overlap rows");
+    DevInfo di;
+    hsa_status_t st = device_info(di);
+    if (st != HSA_OK) return st;
+    if ((st = pending_error()) != HSA_OK) return st;
+    hsa::CompressAppendArgs a{k_new, v_new, B, T, d, new_sb, new_st, pos0, w, m, state_k, state_v, state_sb,
+                              kc, vc, out_sb, out_se, E_cap};
+    return launched(hsa::launch_compress_append(a, dt == HSA_BF16, reinterpret_cast<cudaStream_t>(stream)),
+                    "compress_append");
+}
+
 }  // extern "C"
 
 namespace {

@@ -19,6 +19,19 @@ struct CompressArgs {
     int64_t out_sb, out_se, E_cap;
 };
 cudaError_t launch_compress(const CompressArgs &a, bool bf16, int num_sms, cudaStream_t s);
+struct CompressAppendArgs {
+    const void *k_new, *v_new;  // [B, T, d]
+    int B, T, d;
+    int64_t new_sb, new_st;
+    const int64_t *pos0;        // [B]
+    const float *w;
+    int m;
+    float *state_k, *state_v;   // [B, d] fp32
+    int64_t state_sb;
+    void *kc, *vc;
+    int64_t out_sb, out_se, E_cap;
+};
+cudaError_t launch_compress_append(const CompressAppendArgs &a, bool bf16, cudaStream_t s);
 
 // ---------------------------------------------------------------- indexer
 struct IndexArgs {

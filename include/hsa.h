@@ -109,6 +109,37 @@ HSA_API hsa_status_t hsa_compress(const void *k, const void *v, hsa_dtype_t dt, 
                           hsa_stream_t stream);
 
 /*
+ * hsa_compress_append -- decode-time compression with a partial-block state
+ * cache, the incremental form of hsa_compress (the yage.ai essay
+ * "deepseek-v4-agentic-workload", paragraph on what hybrid attention costs:
+ * V4 manages a state cache beside the classical KV cache; here the state is
+ * the running weighted sum of each sequence's incomplete block).
+ * For each sequence b and new token t = 0..T-1 at position p = pos0[b] + t,
+ * with r = p mod m:
+ *   state[b] = (r == 0 ? 0 : state[b]) + w[r] * x[b, t]   (fp32, fused multiply-add)
+ *   if r == m - 1:  c[b, p / m] = round_to_dt(state[b])
+ * for K (state_k -> kc) and V (state_v -> vc).  The entries are bit-identical
+ * to hsa_compress over the same tokens; earlier tokens are never re-read, so
+ * the raw cache only needs the attention window.  After the call the states
+ * hold the partial sums of each sequence's incomplete block; a state whose
+ * block starts inside the call needs no initial value.
+ *   k_new, v_new  [B, T, d] of `dt`, strides (new_sb, new_st), unit channel stride
+ *   pos0          device int64 [B], >= 0
+ *   w             device fp32 [m]
+ *   state_k, state_v  device fp32 [B, d], sequence stride state_sb (elements),
+ *                 16-byte aligned
+ *   kc, vc        [B, E_cap, d] of `dt`, strides (out_sb, out_se)
+ * The indexer key of a new entry comes from the model's indexer projection,
+ * which this library does not hold: the caller writes it into k_idx.
+ * d a multiple of 8 (bf16) or 4 (fp32), d <= 512; m in [1, 4096].  Entries
+ * beyond E_cap or a negative position raise the device flag.
+ */
+HSA_API hsa_status_t hsa_compress_append(const void *k_new, const void *v_new, hsa_dtype_t dt, int B, int T, int d,
+                                         int64_t new_sb, int64_t new_st, const int64_t *pos0, const float *w, int m,
+                                         float *state_k, float *state_v, int64_t state_sb, void *kc, void *vc,
+                                         int64_t out_sb, int64_t out_se, int64_t E_cap, hsa_stream_t stream);
+
+/*
  * hsa_index_topk -- lightning indexer and exact top-k (QbitAI article,
  * 混合注意力机制: CSA step 2 "a light indexer scores each query token against
  * every compressed block, the top-k blocks are kept"; k = 512 for V4-Flash and
