@@ -60,6 +60,9 @@ def _get():
                                       P, P, I32, I64, I32, D, P, P]
         lib.orc_lse_merge.restype = I32
         lib.orc_lse_merge.argtypes = [I32, P, P, I32, I32, P, P]
+        lib.orc_attn_v4_rows.restype = I32
+        lib.orc_attn_v4_rows.argtypes = [I64, P, I32, P, P, I32, I32, P, I32, I64, I32, P, I32, P, I32, I64, I32,
+                                         D, P, P, D, I32, D, P, P, P]
         _lib = lib
     return _lib
 
@@ -182,3 +185,38 @@ def lse_merge(o_parts, lse_parts):
     lse = np.empty((H,), dtype=np.float64)
     _check(_get().orc_lse_merge(S, _ptr(o), _ptr(ls), H, d, _ptr(out), _ptr(lse)))
     return out, lse
+
+
+def attn_v4_rows(q, row_b, row_p, ent, m, idx, raw, window, scale, gamma_q=None, gamma_kv=None, eps=1e-6,
+                 rope_dims=64, theta=10000.0, sink=None):
+    """V4 attention details (QbitAI article, hybrid attention: the Q/KV normalisation,
+    partial RoPE, shared K=V entry with the output's inverse rotation, and attention
+    sink paragraphs) over the same set as attn_rows.  q: [n_rows, H, d]; ent: [B, E_cap, d]
+    (key and value); raw: [B, N_cap, d]; gamma_*: [d] or None; sink: [H] or None.
+    Returns (out [n_rows, H, d] float64, lse [n_rows, H] float64)."""
+    qa, qdt = _float_arr(q)
+    n_rows, H, d = qa.shape
+    ea, edt = _float_arr(ent)
+    B, E_cap, d2 = ea.shape
+    ra, rdt = _float_arr(raw)
+    _, N_cap, d3 = ra.shape
+    assert d == d2 == d3
+    rb = np.ascontiguousarray(row_b, dtype=np.int64).reshape(n_rows)
+    rp = np.ascontiguousarray(row_p, dtype=np.int64).reshape(n_rows)
+    if idx is None:
+        iptr, topk = None, 0
+    else:
+        ia = np.ascontiguousarray(idx, dtype=np.int32)
+        iptr, topk = _ptr(ia), ia.shape[1]
+    gq = None if gamma_q is None else np.ascontiguousarray(gamma_q, dtype=np.float64)
+    gk = None if gamma_kv is None else np.ascontiguousarray(gamma_kv, dtype=np.float64)
+    sk = None if sink is None else np.ascontiguousarray(sink, dtype=np.float64)
+    out = np.empty((n_rows, H, d), dtype=np.float64)
+    lse = np.empty((n_rows, H), dtype=np.float64)
+    _check(_get().orc_attn_v4_rows(n_rows, _ptr(qa), qdt, _ptr(rb), _ptr(rp), H, d, _ptr(ea), edt, E_cap, m, iptr,
+                                   topk, _ptr(ra), rdt, N_cap, window, float(scale),
+                                   None if gq is None else _ptr(gq), None if gk is None else _ptr(gk), float(eps),
+                                   int(rope_dims), float(theta), None if sk is None else _ptr(sk), _ptr(out),
+                                   _ptr(lse)))
+    return out, lse
+

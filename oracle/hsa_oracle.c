@@ -375,3 +375,146 @@ int orc_lse_merge(int n_parts, const double *o_parts, const double *lse_parts, i
     }
     return ORC_OK;
 }
+
+/* V4's per-layer attention details ([QbitAI] section 混合注意力机制, the paragraphs after
+ * the CSA/HCA description):
+ *   - Q/KV normalisation: before core attention the query and every KV entry go
+ *     through RMSNorm, N(x)_c = gamma_c * x_c / sqrt(mean_c(x_c^2) + eps);
+ *   - partial RoPE: only the last `rd` channels of the query and of the KV entries
+ *     are rotated; channel pair k (channels d-rd+2k, d-rd+2k+1) of a vector at
+ *     position t turns by the angle t * theta^(-2k/rd);
+ *   - a KV entry is both key and value, so the output also gets the rotation of
+ *     position -i (i = the query's position) on the same channels, which leaves
+ *     only relative position;
+ *   - a learnable sink logit z_h joins the softmax denominator.
+ * For query row r (sequence b, position p) and head h, over the same multiset S as
+ * orc_attn_rows (selected or all visible entries, plus raw tokens p-W+1 .. p),
+ * with position t_x = (j+1)*m - 1 for entry j (its block's last token; reading)
+ * and t for raw token t:
+ *   q~ = R(p) N_q(q[r, h]),   e~_x = R(t_x) N_kv(e_x)
+ *   logit_x = scale * <q~, e~_x>,   L = ln(sum_x exp(logit_x) + exp(z_h))
+ *   out = R(-p) sum_x exp(logit_x - L) e~_x,   lse = L.
+ * With S empty and no sink: out = 0, lse = -inf.  ent: [B, E_cap, d] (the shared
+ * K=V entries), raw: [B, N_cap, d]; gamma_q, gamma_kv: [d] or NULL (all ones);
+ * sink: [H] or NULL.
+ * Pinned by: with rd = 0 and unit gamma it equals orc_attn_rows on normalised
+ * inputs; one item gives out = R(t - p) N(e) in closed form; shifting every
+ * position by the same amount leaves the output unchanged; the sink's weight on
+ * one item is exp(l) / (exp(l) + exp(z)). */
+static void orc_norm_rope(const void *x, int dt, int64_t off, int d, const double *gamma, double eps,
+                          int rd, double theta, int64_t pos, double *y)
+{
+    double ss = 0.0;
+    for (int c = 0; c < d; ++c) {
+        double v = orc_load(x, dt, off + c);
+        ss += v * v;
+    }
+    double inv = 1.0 / sqrt(ss / d + eps);
+    for (int c = 0; c < d; ++c)
+        y[c] = (gamma ? gamma[c] : 1.0) * orc_load(x, dt, off + c) * inv;
+    for (int k = 0; k < rd / 2; ++k) {
+        int c0 = d - rd + 2 * k;
+        double ang = (double)pos * pow(theta, -2.0 * k / rd);
+        double u = y[c0], v = y[c0 + 1];
+        y[c0] = u * cos(ang) - v * sin(ang);
+        y[c0 + 1] = u * sin(ang) + v * cos(ang);
+    }
+}
+
+int orc_attn_v4_rows(int64_t n_rows, const void *q, int q_dt, const int64_t *row_b,
+                     const int64_t *row_p, int H, int d, const void *ent, int e_dt, int64_t E_cap,
+                     int m, const int32_t *idx, int topk, const void *raw, int r_dt, int64_t N_cap,
+                     int window, double scale, const double *gamma_q, const double *gamma_kv,
+                     double eps, int rd, double theta, const double *sink, double *out, double *lse)
+{
+    if (n_rows < 0 || H <= 0 || d <= 0 || m <= 0 || window < 0 || (idx && topk < 0) || rd < 0 ||
+        rd > d || rd % 2)
+        return ORC_ERR_ARG;
+    for (int64_t r = 0; r < n_rows; ++r) {
+        int64_t p = row_p[r];
+        if (p < 0 || p >= N_cap || orc_num_entries(p, m) > E_cap)
+            return ORC_ERR_RANGE;
+    }
+    int err = ORC_OK;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t r = 0; r < n_rows; ++r) {
+        int64_t b = row_b[r], p = row_p[r];
+        int64_t E = orc_num_entries(p, m);
+        int64_t t0 = p - window + 1 < 0 ? 0 : p - window + 1;
+        int64_t n_win = window > 0 ? p - t0 + 1 : 0;
+        int64_t n_ent = idx ? topk : E;
+        int64_t n_max = n_ent + n_win;
+        double *items = (double *)malloc(sizeof(double) * (size_t)((n_max + 1) * d));
+        double *logit = (double *)malloc(sizeof(double) * (size_t)(n_max + 1));
+        double *qv = (double *)malloc(sizeof(double) * (size_t)d);
+        if (!items || !logit || !qv) {
+#pragma omp critical
+            err = ORC_ERR_NOMEM;
+            free(items); free(logit); free(qv);
+            continue;
+        }
+        /* the multiset, each item normalised and rotated to its own position */
+        int64_t n = 0;
+        for (int64_t i = 0; i < n_ent; ++i) {
+            int64_t j = idx ? (int64_t)idx[r * topk + i] : i;
+            if (j < 0)
+                continue;
+            if (j >= E) {
+#pragma omp critical
+                err = ORC_ERR_INDEX;
+                continue;
+            }
+            orc_norm_rope(ent, e_dt, (b * E_cap + j) * d, d, gamma_kv, eps, rd, theta, (j + 1) * m - 1,
+                          items + n * d);
+            ++n;
+        }
+        for (int64_t t = t0; t < t0 + n_win; ++t) {
+            orc_norm_rope(raw, r_dt, (b * N_cap + t) * d, d, gamma_kv, eps, rd, theta, t, items + n * d);
+            ++n;
+        }
+        for (int h = 0; h < H; ++h) {
+            orc_norm_rope(q, q_dt, (r * H + h) * (int64_t)d, d, gamma_q, eps, rd, theta, p, qv);
+            double z = sink ? sink[h] : -INFINITY;
+            double M = z;
+            for (int64_t x = 0; x < n; ++x) {
+                double dot = 0.0;
+                for (int c = 0; c < d; ++c)
+                    dot += qv[c] * items[x * d + c];
+                logit[x] = scale * dot;
+                if (logit[x] > M)
+                    M = logit[x];
+            }
+            double *o = out + (r * H + h) * (int64_t)d;
+            if (M == -INFINITY) {
+                for (int c = 0; c < d; ++c)
+                    o[c] = 0.0;
+                if (lse)
+                    lse[r * H + h] = -INFINITY;
+                continue;
+            }
+            double Lsum = z == -INFINITY ? 0.0 : exp(z - M);
+            for (int64_t x = 0; x < n; ++x)
+                Lsum += exp(logit[x] - M);
+            double L = M + log(Lsum);
+            for (int c = 0; c < d; ++c) {
+                double acc = 0.0;
+                for (int64_t x = 0; x < n; ++x)
+                    acc += exp(logit[x] - L) * items[x * d + c];
+                o[c] = acc;
+            }
+            /* the rotation of position -p on the same channels */
+            for (int k = 0; k < rd / 2; ++k) {
+                int c0 = d - rd + 2 * k;
+                double ang = -(double)p * pow(theta, -2.0 * k / rd);
+                double u = o[c0], v = o[c0 + 1];
+                o[c0] = u * cos(ang) - v * sin(ang);
+                o[c0 + 1] = u * sin(ang) + v * cos(ang);
+            }
+            if (lse)
+                lse[r * H + h] = L;
+        }
+        free(items); free(logit); free(qv);
+    }
+    return err;
+}
+

@@ -439,3 +439,94 @@ def test_pipeline_tiny_against_textbook():
         ref = _sdpa(q[p:p + 1], keys, vals, mask)
         np.testing.assert_allclose(out[p], ref[0], atol=1e-12)
         assert sorted(order) == idx[p][:cnt[p]].tolist()
+
+
+# ------------------------------------------------ V4 attention details ---
+# (QbitAI article, hybrid attention: the Q/KV normalisation, partial RoPE, shared
+# K=V entry with the output's inverse rotation, and attention sink paragraphs)
+
+def _rms(x, gamma=None, eps=1e-6):
+    x = np.asarray(x, dtype=np.float64)
+    y = x / np.sqrt((x * x).mean(-1, keepdims=True) + eps)
+    return y if gamma is None else y * gamma
+
+
+def _rot(x, pos, rd, theta=10000.0):
+    """rotate channel pairs (d-rd+2k, d-rd+2k+1) by pos * theta^(-2k/rd) (numpy, complex form)"""
+    x = np.array(x, dtype=np.float64)
+    d = x.shape[-1]
+    k = np.arange(rd // 2)
+    ang = np.asarray(pos, dtype=np.float64)[..., None] * theta ** (-2.0 * k / rd)
+    z = (x[..., d - rd::2] + 1j * x[..., d - rd + 1::2]) * np.exp(1j * ang)
+    x[..., d - rd::2], x[..., d - rd + 1::2] = z.real, z.imag
+    return x
+
+
+def _v4_case(seed, B=1, E_cap=16, m=4, H=3, d=16, N=None):
+    g = np.random.default_rng(seed)
+    N = N or E_cap * m
+    return (g.standard_normal((B, 1, H, d)), g.standard_normal((B, E_cap, d)) * 3,
+            g.standard_normal((B, N, d)) * 2, g.uniform(0.5, 1.5, d), g.uniform(0.5, 1.5, d))
+
+
+def test_v4_without_rope_is_plain_attention_on_normalised_inputs():
+    q, ent, raw, gq, gk = _v4_case(1)
+    m, W, p = 4, 5, 50
+    o, l = oracle.attn_v4_rows(q[0], [0], [p], ent, m, None, raw, W, 0.3, gq, gk, 1e-6, 0, 10000.0, None)
+    ro, rl = oracle.attn_rows(_rms(q[0], gq), [0], [p], _rms(ent, gk), _rms(ent, gk), m, None, _rms(raw, gk),
+                              _rms(raw, gk), W, 0.3)
+    np.testing.assert_allclose(o, ro, atol=1e-12)
+    np.testing.assert_allclose(l, rl, atol=1e-12)
+
+
+@pytest.mark.parametrize("rd", [2, 8, 16])
+def test_v4_one_item_is_relative_rotation(rd):
+    """one attended entry: softmax weight 1, out = R(t - p) N(e) in closed form"""
+    q, ent, raw, gq, gk = _v4_case(2)
+    m, p, j = 4, 61, 9
+    idx = np.full((1, 4), -1, np.int32)
+    idx[0, 2] = j
+    o, l = oracle.attn_v4_rows(q[0], [0], [p], ent, m, idx, raw, 0, 0.7, gq, gk, 1e-6, rd, 10000.0, None)
+    t = (j + 1) * m - 1
+    want = _rot(_rms(ent[0, j], gk), t - p, rd)
+    for h in range(q.shape[2]):
+        np.testing.assert_allclose(o[0, h], want, atol=1e-12)
+        qv = _rot(_rms(q[0, 0, h], gq), p, rd)
+        kv = _rot(_rms(ent[0, j], gk), t, rd)
+        assert abs(l[0, h] - 0.7 * qv @ kv) < 1e-12
+
+
+def test_v4_shift_of_every_position_leaves_output_unchanged():
+    """window-only attention at positions p and p + shift over the same token vectors"""
+    g = np.random.default_rng(3)
+    d, H, W, shift = 16, 2, 6, 37
+    q = g.standard_normal((1, H, d))
+    toks = g.standard_normal((W, d))
+    N = 200
+    ent = np.zeros((1, N, d))
+    outs = []
+    for p in (80, 80 + shift):
+        raw = np.zeros((1, N, d))
+        raw[0, p - W + 1:p + 1] = toks
+        outs.append(oracle.attn_v4_rows(q, [0], [p], ent, 1, np.full((1, 1), -1, np.int32), raw, W, 0.25,
+                                        None, None, 1e-6, 16, 10000.0, None)[0])
+    np.testing.assert_allclose(outs[0], outs[1], atol=1e-10)
+
+
+def test_v4_sink_weight_closed_form_and_limit():
+    q, ent, raw, gq, gk = _v4_case(4)
+    m, p, j = 4, 40, 3
+    idx = np.array([[j]], np.int32)
+    base, bl = oracle.attn_v4_rows(q[0], [0], [p], ent, m, idx, raw, 0, 0.5, gq, gk, 1e-6, 8, 10000.0, None)
+    z = np.array([0.3, -1.0, 2.0])
+    o, l = oracle.attn_v4_rows(q[0], [0], [p], ent, m, idx, raw, 0, 0.5, gq, gk, 1e-6, 8, 10000.0, z)
+    w = np.exp(bl[0]) / (np.exp(bl[0]) + np.exp(z))           # one item: weight e^l / (e^l + e^z)
+    np.testing.assert_allclose(o[0], base[0] * w[:, None], atol=1e-12)
+    np.testing.assert_allclose(l[0], np.logaddexp(bl[0], z), atol=1e-12)
+    o2, l2 = oracle.attn_v4_rows(q[0], [0], [p], ent, m, idx, raw, 0, 0.5, gq, gk, 1e-6, 8, 10000.0,
+                                 np.full(3, -np.inf))
+    np.testing.assert_allclose(o2, base, atol=0)
+    # sink only (empty set): out 0, lse = z
+    o3, l3 = oracle.attn_v4_rows(q[0], [0], [p], ent, m, np.full((1, 1), -1, np.int32), raw, 0, 0.5, gq, gk,
+                                 1e-6, 8, 10000.0, z)
+    assert not o3.any() and np.allclose(l3[0], z)
