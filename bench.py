@@ -337,6 +337,48 @@ def time_state_append(bench, steps: int = 64, reps: int = 20) -> float:
     return t0.elapsed_time(t1) / (reps * steps)
 
 
+def time_v4_details(bench, steps: int = 64, reps: int = 20) -> dict:
+    """ms per call of the V4-detail kernels a decode step adds around the same attention
+    kernels: RMSNorm + partial RoPE of the step's queries and of each sequence's new
+    entry, and the sink + inverse rotation of the output (CUDA graphs of `steps` calls)."""
+    wl, L, dev = bench.wl, bench.L, bench.dev
+    B, H, d, m = wl.B, wl.H, wl.d, wl.m
+    q = bench.q[0].clone()
+    zeros = torch.zeros(B, dtype=torch.int64, device=dev)
+    ones = torch.ones(B, dtype=torch.int64, device=dev)
+    pos = bench.ctx - 1
+    E_new = torch.div(bench.ctx, m, rounding_mode="floor")
+    gamma = torch.ones(d, device=dev)
+    sink = torch.zeros(H, device=dev)
+    out = bench.out[0].clone()
+    lse = torch.zeros((B, H), dtype=torch.float32, device=dev)
+    kc = bench.kc.clone()
+    calls = {
+        "v4_prep_query": lambda: L.hsa_rmsnorm_rope(q.view(B, 1, H, d), zeros, ones, 1, pos, 1, 0, gamma),
+        "v4_prep_entry": lambda: L.hsa_rmsnorm_rope(kc, E_new - 1, E_new, 1, None, m, m - 1, gamma),
+        "v4_finalize": lambda: L.hsa_attn_finalize(out, lse, pos, sink),
+    }
+    res = {}
+    for name, fn in calls.items():
+        g = torch.cuda.CUDAGraph()
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.graph(g, stream=s):
+            for _ in range(steps):
+                fn()
+        torch.cuda.current_stream().wait_stream(s)
+        g.replay()
+        torch.cuda.synchronize()
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record()
+        for _ in range(reps):
+            g.replay()
+        t1.record()
+        torch.cuda.synchronize()
+        res[name] = t0.elapsed_time(t1) / (reps * steps)
+    return res
+
+
 def run_hsa(args, ws, rank, local):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
@@ -390,6 +432,7 @@ def run_hsa(args, ws, rank, local):
             per_op["attn_decode"].append(ev[i][2].elapsed_time(ev[i][3]))
     op_ms = {k: statistics.fmean(v) for k, v in per_op.items()}
     op_ms["compress_append"] = time_state_append(bench)
+    op_ms.update(time_v4_details(bench))
 
     cnt_total = int(sum(int(c.sum()) for c in bench.cnt[:1]))
     bytes_ = algorithmic_bytes(WL, cnt_total)

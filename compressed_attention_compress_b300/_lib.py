@@ -25,7 +25,7 @@ _STATUS = {0: "HSA_OK", 1: "HSA_ERR_INVALID_ARG", 2: "HSA_ERR_UNSUPPORTED", 3: "
 EXPORTS = ["hsa_last_error", "hsa_version", "hsa_check", "hsa_compress", "hsa_compress_append", "hsa_index_topk_workspace_size",
            "hsa_index_topk", "hsa_index_topk_noalloc", "hsa_attn_decode_workspace_size", "hsa_attn_decode",
            "hsa_attn_prefill_workspace_size", "hsa_attn_prefill", "hsa_index_scores", "hsa_topk_merge",
-           "hsa_lse_merge"]
+           "hsa_lse_merge", "hsa_rmsnorm_rope", "hsa_attn_finalize"]
 NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
@@ -71,6 +71,10 @@ def _load():
     lib.hsa_topk_merge.argtypes = [P, P, I, I, I, P, P, P]
     lib.hsa_lse_merge.restype = I
     lib.hsa_lse_merge.argtypes = [P, P, I, I, I, I, I, P, P, P]
+    lib.hsa_rmsnorm_rope.restype = I
+    lib.hsa_rmsnorm_rope.argtypes = [P, I, I, I, I, I64, I64, I64, P, P, I64, P, I64, I64, P, F, I, F, P]
+    lib.hsa_attn_finalize.restype = I
+    lib.hsa_attn_finalize.argtypes = [P, P, I, I, I, I, I, P, P, I, F, P]
     return lib
 
 
@@ -207,6 +211,32 @@ def hsa_lse_merge(parts_o, parts_lse, out, lse_out=None, stream=None):
     S, rows, H, d = parts_o.shape
     _chk(lib.hsa_lse_merge(_p(parts_o), _p(parts_lse), _dt(parts_o), S, rows, H, d, _p(out), _p(lse_out),
                            _stream(stream)))
+
+
+def hsa_rmsnorm_rope(x, n_begin, n_end, max_rows, pos_base=None, pos_stride=1, pos_offset=0, gamma=None,
+                     eps=1e-6, rope_dims=64, theta=10000.0, stream=None):
+    """In place x <- R(pos) RMSNorm(x) on rows [n_begin[b], n_end[b]) of x [B, n_cap, d] or [B, n_cap, H, d];
+    pos = pos_base[b] + n * pos_stride + pos_offset."""
+    if x.dim() == 3:
+        B, n_cap, d = x.shape
+        H = 1
+    else:
+        B, n_cap, H, d = x.shape
+        assert x.stride(2) == d
+    _chk(lib.hsa_rmsnorm_rope(_p(x), _dt(x), B, H, d, x.stride(0), x.stride(1), n_cap, _p(n_begin), _p(n_end),
+                              int(max_rows), _p(pos_base), int(pos_stride), int(pos_offset), _p(gamma), float(eps),
+                              int(rope_dims), float(theta), _stream(stream)))
+
+
+def hsa_attn_finalize(out, lse, q_pos0, sink=None, rope_dims=64, theta=10000.0, stream=None):
+    """Sink and inverse rotation on (out [B, T, H, d] or [B, H, d], lse) in place; p = q_pos0[b] + t."""
+    if out.dim() == 3:
+        B, H, d = out.shape
+        T = 1
+    else:
+        B, T, H, d = out.shape
+    _chk(lib.hsa_attn_finalize(_p(out), _p(lse), _dt(out), B, T, H, d, _p(q_pos0), _p(sink), int(rope_dims),
+                               float(theta), _stream(stream)))
 
 
 def workspace(nbytes: int, device="cuda"):

@@ -1,6 +1,7 @@
 // C-ABI layer: argument validation, workspace carving and launch sequencing.
 // Every entry point enqueues on the caller's stream and never allocates,
 // frees or synchronises (hsa_check excepted).
+#include <math.h>
 #include <stdarg.h>
 #include <stdio.h>
 #include <string.h>
@@ -531,6 +532,53 @@ hsa_status_t hsa_lse_merge(const void *parts_o, const float *parts_lse, hsa_dtyp
     if ((st = pending_error()) != HSA_OK) return st;
     hsa::LseMergeArgs a{parts_o, parts_lse, S, rows, H, d, out, lse_out};
     return launched(hsa::launch_lse_merge(a, dt == HSA_BF16, reinterpret_cast<cudaStream_t>(stream)), "lse_merge");
+}
+
+hsa_status_t hsa_rmsnorm_rope(void *x, hsa_dtype_t dt, int B, int H, int d, int64_t x_sb, int64_t x_sn,
+                              int64_t n_cap, const int64_t *n_begin, const int64_t *n_end, int64_t max_rows,
+                              const int64_t *pos_base, int64_t pos_stride, int64_t pos_offset, const float *gamma,
+                              float eps, int rope_dims, float theta, hsa_stream_t stream) {
+    if (!dtype_ok(dt)) return fail(HSA_ERR_UNSUPPORTED, "dtype %d", (int)dt);
+    if (B < 0 || H <= 0 || d <= 0 || n_cap < 0 || max_rows < 0 || !(eps >= 0.f) || rope_dims < 0 || !(theta > 0.f))
+        return fail(HSA_ERR_INVALID_ARG, "bad size or parameter");
+    if (d % 64 || d > 512) return fail(HSA_ERR_UNSUPPORTED, "d must be a multiple of 64 up to 512, got %d", d);
+    if (rope_dims % 2 || rope_dims > d) return fail(HSA_ERR_INVALID_ARG, "rope_dims must be even and <= d");
+    if (rope_dims > hsa::kMaxRopeDims) return fail(HSA_ERR_UNSUPPORTED, "rope_dims above %d", hsa::kMaxRopeDims);
+    if (B == 0 || max_rows == 0) return ok();
+    if (B > 65535) return fail(HSA_ERR_UNSUPPORTED, "more than 65535 sequences");
+    if (!x || !n_begin || !n_end) return fail(HSA_ERR_INVALID_ARG, "null pointer");
+    if (x_sn < (int64_t)H * d || x_sb < 0) return fail(HSA_ERR_INVALID_ARG, "row strides overlap rows");
+    DevInfo di;
+    hsa_status_t st = device_info(di);
+    if (st != HSA_OK) return st;
+    if ((st = pending_error()) != HSA_OK) return st;
+    hsa::NormRopeArgs a{x, B, H, d, x_sb, x_sn, n_cap, n_begin, n_end, max_rows, pos_base, pos_stride, pos_offset,
+                        gamma, eps, rope_dims, {}};
+    for (int k = 0; k < rope_dims / 2; ++k) a.inv_freq[k] = pow((double)theta, -2.0 * k / rope_dims);
+    return launched(hsa::launch_rmsnorm_rope(a, dt == HSA_BF16, reinterpret_cast<cudaStream_t>(stream)),
+                    "rmsnorm_rope");
+}
+
+hsa_status_t hsa_attn_finalize(void *out, float *lse, hsa_dtype_t dt, int B, int T, int H, int d,
+                               const int64_t *q_pos0, const float *sink, int rope_dims, float theta,
+                               hsa_stream_t stream) {
+    if (!dtype_ok(dt)) return fail(HSA_ERR_UNSUPPORTED, "dtype %d", (int)dt);
+    if (B < 0 || T < 0 || H <= 0 || d <= 0 || rope_dims < 0 || !(theta > 0.f))
+        return fail(HSA_ERR_INVALID_ARG, "bad size or parameter");
+    if (d % 64 || d > 512) return fail(HSA_ERR_UNSUPPORTED, "d must be a multiple of 64 up to 512, got %d", d);
+    if (rope_dims % 2 || rope_dims > d) return fail(HSA_ERR_INVALID_ARG, "rope_dims must be even and <= d");
+    if (rope_dims > hsa::kMaxRopeDims) return fail(HSA_ERR_UNSUPPORTED, "rope_dims above %d", hsa::kMaxRopeDims);
+    if (B * (int64_t)T == 0) return ok();
+    if (B * (int64_t)T > 65535) return fail(HSA_ERR_UNSUPPORTED, "more than 65535 query rows");
+    if (!out || !q_pos0 || (sink && !lse)) return fail(HSA_ERR_INVALID_ARG, "null pointer (a sink needs lse)");
+    DevInfo di;
+    hsa_status_t st = device_info(di);
+    if (st != HSA_OK) return st;
+    if ((st = pending_error()) != HSA_OK) return st;
+    hsa::FinalizeArgs a{out, lse, B, T, H, d, q_pos0, sink, rope_dims, {}};
+    for (int k = 0; k < rope_dims / 2; ++k) a.inv_freq[k] = pow((double)theta, -2.0 * k / rope_dims);
+    return launched(hsa::launch_attn_finalize(a, dt == HSA_BF16, reinterpret_cast<cudaStream_t>(stream)),
+                    "attn_finalize");
 }
 
 }  // extern "C"

@@ -107,6 +107,33 @@ struct LseMergeArgs {
 };
 cudaError_t launch_lse_merge(const LseMergeArgs &a, bool bf16, cudaStream_t s);
 
+// ------------------------------------------- V4 attention details (v4_extras.cu)
+constexpr int kMaxRopeDims = 128;
+struct NormRopeArgs {
+    void *x;                  // [B, n_cap, H, d], strides (x_sb, x_sn), heads contiguous
+    int B, H, d;
+    int64_t x_sb, x_sn, n_cap;
+    const int64_t *n_begin, *n_end;  // [B]
+    int64_t max_rows;
+    const int64_t *pos_base;  // [B] or null (0)
+    int64_t pos_stride, pos_offset;
+    const float *gamma;       // [d] or null (1)
+    float eps;
+    int rope_dims;
+    double inv_freq[kMaxRopeDims / 2];  // theta^(-2k/rope_dims)
+};
+cudaError_t launch_rmsnorm_rope(const NormRopeArgs &a, bool bf16, cudaStream_t s);
+struct FinalizeArgs {
+    void *out;                // [B*T, H, d]
+    float *lse;               // [B*T, H]
+    int B, T, H, d;
+    const int64_t *q_pos0;    // [B]
+    const float *sink;        // [H] or null
+    int rope_dims;
+    double inv_freq[kMaxRopeDims / 2];
+};
+cudaError_t launch_attn_finalize(const FinalizeArgs &a, bool bf16, cudaStream_t s);
+
 // -------------------------------------------------------------- attention
 struct AttnArgs {
     const void *q;      // [rows, H, d]

@@ -257,6 +257,49 @@ HSA_API hsa_status_t hsa_attn_prefill(const void *q, hsa_dtype_t dt, int B, int 
                               hsa_stream_t stream);
 
 /*
+ * V4's per-layer attention details (QbitAI article, 混合注意力机制, the
+ * paragraphs after the CSA/HCA description: Q/KV normalisation, partial RoPE,
+ * one KV entry as key and value with the output rotated back by the query's
+ * position, attention sink).  They run on the same attention kernels: prepare
+ * the query, the compressed entries and the raw window tokens with
+ * hsa_rmsnorm_rope, pass one buffer as both kc and vc (and as both k_raw and
+ * v_raw), request lse from the attention call, then apply hsa_attn_finalize.
+ * The result is
+ *   q~ = R(p) N_q(q),  e~_x = R(t_x) N_kv(e_x),  logit_x = scale <q~, e~_x>,
+ *   out = R(-p) sum_x softmax'(logit)_x e~_x,  lse = ln(sum_x e^logit_x + e^z_h)
+ * where softmax' includes the sink logit z_h in its denominator, N is RMSNorm
+ * x * gamma / sqrt(mean(x^2) + eps), and R(t) turns channel pair k of the last
+ * rope_dims channels (channels d - rope_dims + 2k, + 1) by t * theta^(-2k /
+ * rope_dims).  A compressed entry j sits at its block's last token, (j+1)*m - 1.
+ *
+ * hsa_rmsnorm_rope -- x <- R(pos) N(x), in place, for the rows
+ * n in [n_begin[b], n_end[b]) of every sequence b and all H heads:
+ *   x          [B, n_cap, H, d] of `dt`, strides (x_sb, x_sn) in elements,
+ *              heads contiguous (stride d)
+ *   n_begin, n_end  device int64 [B];  max_rows host bound on n_end - n_begin
+ *   pos        (pos_base ? pos_base[b] : 0) + n * pos_stride + pos_offset
+ *              (queries: pos_base = q_pos0, stride 1; entries: stride m,
+ *              offset m - 1; raw tokens: stride 1)
+ *   gamma      device fp32 [d] or NULL (ones);  rope_dims even, <= min(d, 128)
+ * d a multiple of 64, d <= 512.  Rows outside [0, n_cap) raise the device flag.
+ *
+ * hsa_attn_finalize -- sink and inverse rotation on the (out, lse) of an
+ * attention call over prepared vectors, in place:
+ *   lse' = ln(e^lse + e^sink[h]),  out' = R(-p) e^(lse - lse') out
+ * with p = q_pos0[b] + t (decode: q_pos0 = ctx_len - 1, T = 1).
+ *   out        [B, T, H, d] of `dt`, contiguous;  lse fp32 [B, T, H]
+ *   sink       device fp32 [H] or NULL (no sink: lse unchanged)
+ */
+HSA_API hsa_status_t hsa_rmsnorm_rope(void *x, hsa_dtype_t dt, int B, int H, int d, int64_t x_sb, int64_t x_sn,
+                                      int64_t n_cap, const int64_t *n_begin, const int64_t *n_end,
+                                      int64_t max_rows, const int64_t *pos_base, int64_t pos_stride,
+                                      int64_t pos_offset, const float *gamma, float eps, int rope_dims,
+                                      float theta, hsa_stream_t stream);
+HSA_API hsa_status_t hsa_attn_finalize(void *out, float *lse, hsa_dtype_t dt, int B, int T, int H, int d,
+                                       const int64_t *q_pos0, const float *sink, int rope_dims, float theta,
+                                       hsa_stream_t stream);
+
+/*
  * Context-parallel exchange of one long sequence (no counterpart in the pages:
  * the pages describe one GPU's attention; these three calls let several ranks
  * that each hold a contiguous range of a sequence's compressed entries produce
