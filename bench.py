@@ -310,6 +310,26 @@ def capture_block(bench, steps, start, events=None):
     return g
 
 
+def time_graph(fn, R: int, steps: int = 64, reps: int = 20) -> float:
+    """ms per call of fn(replica) in a CUDA graph of `steps` calls over R replicas."""
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.graph(g, stream=s):
+        for i in range(steps):
+            fn(i % R)
+    torch.cuda.current_stream().wait_stream(s)
+    g.replay()
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for _ in range(reps):
+        g.replay()
+    t1.record()
+    torch.cuda.synchronize()
+    return t0.elapsed_time(t1) / (reps * steps)
+
+
 def time_state_append(bench, steps: int = 64, reps: int = 20) -> float:
     """ms per call of the state-cache form of the step's compression (hsa_compress_append:
     one new token per sequence, completing its block), in a CUDA graph of `steps` calls."""
@@ -433,6 +453,9 @@ def run_hsa(args, ws, rank, local):
     op_ms = {k: statistics.fmean(v) for k, v in per_op.items()}
     op_ms["compress_append"] = time_state_append(bench)
     op_ms.update(time_v4_details(bench))
+    op_ms["attn_decode_shared_kv"] = time_graph(lambda r: bench.L.hsa_attn_decode(
+        bench.q[r], bench.kc, bench.kc, WL.m, bench.idx[r].view(WL.B, WL.topk), bench.cnt[r].view(WL.B),
+        bench.k_raw, bench.k_raw, WL.window, bench.ctx, WL.scale, bench.out[r], bench.lse[r], bench.ws_a), bench.R)
 
     cnt_total = int(sum(int(c.sum()) for c in bench.cnt[:1]))
     bytes_ = algorithmic_bytes(WL, cnt_total)
@@ -581,6 +604,9 @@ def run_prefill(dev, reps: int):
         flop = prefill_flops(wl)
         r["attn_tflops"] = flop / (r["attn_ms"] * 1e-3) / 1e12
         r["attn_frac_of_bf16_peak"] = r["attn_tflops"] / peak_tc[0]
+        # V4's shared key/value entry: one buffer passed as both K and V (each item loaded once)
+        r["attn_shared_kv_ms"] = timed(lambda: L.hsa_attn_prefill(q, kc, kc, m, idx, cnt, kr, kr, wl.window, pos0,
+                                                                  wl.scale, out, ws=ws_a))
         if wl.kind == "csa":
             gather = float(B * T) * (wl.topk + wl.window) * 2 * d * 2
             r["attn_gather_gbs"] = gather / (r["attn_ms"] * 1e-3) / 1e9

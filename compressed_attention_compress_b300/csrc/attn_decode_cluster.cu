@@ -19,7 +19,9 @@
 //
 // For CSA the item space is static (topk slots + window slots; slots past cnt
 // or holding -1 are masked), so the index loads are issued together with the
-// position load, one memory round trip before the gathers.
+// position load, one memory round trip before the gathers.  When the caller
+// passes one buffer as both K and V (V4's shared key/value entry), only one copy
+// of each item is gathered.
 #include <math.h>
 
 #include "common.cuh"
@@ -180,7 +182,9 @@ __global__ void __launch_bounds__(NW * 32) attn_decode_cluster_kernel(AttnArgs a
                 const int64_t off = ent < 0 ? 0 : (ent & ~kRawBit);
                 const int nb = ent < 0 ? 0 : 16;
                 cp_async_16(smem_u32(sK + buf * kStage * D * 2 + swz<D>(it, cc)), (raw ? kr : kc) + off + cc * 8, nb);
-                cp_async_16(smem_u32(sV + buf * kStage * D * 2 + swz<D>(it, cc)), (raw ? vr : vc) + off + cc * 8, nb);
+                if (!a.shared_kv)  // one entry as key and value: the K copy serves both
+                    cp_async_16(smem_u32(sV + buf * kStage * D * 2 + swz<D>(it, cc)), (raw ? vr : vc) + off + cc * 8,
+                                nb);
             }
         }
         cp_async_commit();
@@ -211,7 +215,7 @@ __global__ void __launch_bounds__(NW * 32) attn_decode_cluster_kernel(AttnArgs a
         cp_async_wait<1>();
         __syncthreads();
         const unsigned char *tK = sK + buf * kStage * D * 2;
-        const unsigned char *tV = sV + buf * kStage * D * 2;
+        const unsigned char *tV = a.shared_kv ? tK : sV + buf * kStage * D * 2;
         float s[kStage / 8][4];
 #pragma unroll
         for (int n = 0; n < kStage / 8; ++n) s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.f;

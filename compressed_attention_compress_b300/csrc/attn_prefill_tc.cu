@@ -24,7 +24,8 @@
 //              so that while one tile's softmax runs the tensor core works on
 //              the other tile; completion via tcgen05.commit.
 //   warp 9     TMA producer (one thread): both Q tiles, then K_0, V_0, K_1, V_1,
-//              ... through a 4-slot ring of 32 KiB shared-memory tiles.
+//              ... through a 4-slot ring of 32 KiB shared-memory tiles (only K_j
+//              when one buffer is both K and V, V4's shared key/value entry).
 // All waits are bounded; a wait that gives up raises the device flag and the
 // CTA stops issuing work.
 #include <math.h>
@@ -60,6 +61,7 @@ struct PrefillTcArgs {
     __nv_bfloat16 *out;
     float *lse;
     int tiles_per_seq, pairs_per_seq, n_pairs;
+    int shared_kv;  // one buffer is both K and V: each item tile is loaded once
 };
 
 struct __align__(8) Bars {
@@ -198,7 +200,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                 ++q_issued;
                 const int n_kv = pi.n_ent + pi.n_win;
                 for (int j = 0; j < n_kv && ok; ++j) {
-                    for (int kv = 0; kv < 2 && ok; ++kv, ++u) {
+                    for (int kv = 0; kv < (a.shared_kv ? 1 : 2) && ok; ++kv, ++u) {
                         const int slot = (int)(u % kRing);
                         if (u >= kRing) ok = wait_bar(&bars.kv_empty[slot], (unsigned)(((u / kRing) - 1) & 1), &s_abort);
                         if (!ok) break;
@@ -272,16 +274,19 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                 }
                 // S_X(0) for both tiles
                 uint32_t aK = wait_kv(u);
+                int64_t uk = u++;
                 if (!ok) break;
                 tc::fence_after();
                 for (int x = 0; x < nx; ++x) issue_s(x, aK);
-                tc::commit(&bars.kv_empty[u % kRing]);
-                ++u;
+                if (!a.shared_kv) tc::commit(&bars.kv_empty[uk % kRing]);  // shared: K_0 is also V_0
                 for (int j = 0; j < n_kv && ok; ++j) {
-                    const uint32_t aV = wait_kv(u);
-                    const int64_t uv = u++;
-                    uint32_t aKn = 0;
-                    int64_t uk = -1;
+                    // V_j: its own tile, or K_j itself when one buffer is both
+                    uint32_t aV = aK;
+                    int64_t uv = uk;
+                    if (!a.shared_kv) {
+                        aV = wait_kv(u);
+                        uv = u++;
+                    }
                     for (int x = 0; x < nx && ok; ++x) {
                         ok = wait_bar(&bars.p_full[x], (unsigned)(g[x] & 1), &s_abort);
                         if (ok && j == 0 && pairs_x[x] > 0)
@@ -293,13 +298,13 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                         if (x == nx - 1) tc::commit(&bars.kv_empty[uv % kRing]);
                         if (j + 1 < n_kv) {
                             if (x == 0) {
-                                aKn = wait_kv(u);
+                                aK = wait_kv(u);
                                 uk = u++;
                                 if (!ok) break;
                                 tc::fence_after();
                             }
-                            issue_s(x, aKn);
-                            if (x == nx - 1) tc::commit(&bars.kv_empty[uk % kRing]);
+                            issue_s(x, aK);
+                            if (x == nx - 1 && !a.shared_kv) tc::commit(&bars.kv_empty[uk % kRing]);
                         }
                     }
                 }
@@ -536,6 +541,7 @@ cudaError_t launch_attn_prefill_tc(const AttnArgs &a, int num_sms, cudaStream_t 
     p.tiles_per_seq = (int)(((int64_t)a.T * a.H) / kRows);
     p.pairs_per_seq = (p.tiles_per_seq + 1) / 2;
     p.n_pairs = B * p.pairs_per_seq;
+    p.shared_kv = a.shared_kv;
     static unsigned long long done = 0;
     cudaError_t e = smem_limit_once(attn_prefill_tc_kernel, (int)kSmemBytes, done);
     if (e != cudaSuccess) return e;

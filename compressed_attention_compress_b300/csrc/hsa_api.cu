@@ -356,6 +356,7 @@ hsa_status_t hsa_attn_decode(const void *q, hsa_dtype_t dt, int B, int H, int d,
     a.idx = idx; a.cnt = cnt; a.topk = dense ? 0 : topk;
     a.k_raw = k_raw; a.v_raw = v_raw; a.r_sb = r_sb; a.r_st = r_st; a.N_cap = N_cap; a.window = window;
     a.pos = ctx_len; a.pos_is_ctx = 1; a.scale = scale; a.out = out; a.lse = lse;
+    a.shared_kv = kc == vc && k_raw == v_raw;
     a.split = p.split; a.max_splits = p.max_splits;
     a.part_o = p.total ? reinterpret_cast<float *>(static_cast<char *>(ws) + p.off_o) : nullptr;
     a.part_lse = p.total ? reinterpret_cast<float *>(static_cast<char *>(ws) + p.off_lse) : nullptr;
@@ -395,6 +396,7 @@ hsa_status_t hsa_attn_prefill(const void *q, hsa_dtype_t dt, int B, int T, int H
     a.idx = idx; a.cnt = cnt; a.topk = dense ? 0 : topk;
     a.k_raw = k_raw; a.v_raw = v_raw; a.r_sb = r_sb; a.r_st = r_st; a.N_cap = N_cap; a.window = window;
     a.pos = q_pos0; a.pos_is_ctx = 0; a.scale = scale; a.out = out; a.lse = lse;
+    a.shared_kv = kc == vc && k_raw == v_raw;
     a.split = 0; a.max_splits = 1;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (dt == HSA_BF16 && hsa::prefill_tc_supported(a))

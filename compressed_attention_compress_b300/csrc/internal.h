@@ -151,6 +151,7 @@ struct AttnArgs {
     int window;
     const int64_t *pos;  // decode: ctx_len[b] (p = ctx_len - 1); prefill: q_pos0[b] (p = q_pos0 + t)
     int pos_is_ctx;
+    int shared_kv;      // kc == vc and k_raw == v_raw: one entry is both key and value
     float scale;
     void *out;          // [rows, H, d]
     float *lse;         // [rows, H] or null
