@@ -60,6 +60,8 @@ def _get():
                                       P, P, I32, I64, I32, D, P, P]
         lib.orc_lse_merge.restype = I32
         lib.orc_lse_merge.argtypes = [I32, P, P, I32, I32, P, P]
+        lib.orc_compress_learned.restype = I32
+        lib.orc_compress_learned.argtypes = [P, P, I32, I32, I64, I32, P, P, I32, I32, P, P, P, P, I32, I64]
         lib.orc_attn_v4_rows.restype = I32
         lib.orc_attn_v4_rows.argtypes = [I64, P, I32, P, P, I32, I32, P, I32, I64, I32, P, I32, P, I32, I64, I32,
                                          D, P, P, D, I32, D, P, P, P]
@@ -219,4 +221,25 @@ def attn_v4_rows(q, row_b, row_p, ent, m, idx, raw, window, scale, gamma_q=None,
                                    int(rope_dims), float(theta), None if sk is None else _ptr(sk), _ptr(out),
                                    _ptr(lse)))
     return out, lse
+
+
+def compress_learned(k, v, u, bias, m, L, tok_begin, tok_end, E_cap, out_dtype=np.float64):
+    """Learned, attention-like compression (QbitAI article, hybrid attention: CSA step 1
+    and the HCA paragraph; the window/score reading is stated in hsa_oracle.c).
+    k, v: [B, N_cap, d]; u: [d]; bias: [L].  Returns (kc, vc) [B, E_cap, d]."""
+    ka, kdt = _float_arr(k)
+    va, vdt = _float_arr(v)
+    assert kdt == vdt and ka.shape == va.shape
+    B, N_cap, d = ka.shape
+    ua = np.ascontiguousarray(u, dtype=np.float64)
+    ba = np.ascontiguousarray(bias, dtype=np.float64)
+    assert ua.shape == (d,) and ba.shape == (L,)
+    tb = np.ascontiguousarray(tok_begin, dtype=np.int64)
+    te = np.ascontiguousarray(tok_end, dtype=np.int64)
+    kc = np.zeros((B, E_cap, d), dtype=out_dtype)
+    vc = np.zeros((B, E_cap, d), dtype=out_dtype)
+    code = 2 if out_dtype == np.float64 else 0
+    _check(_get().orc_compress_learned(_ptr(ka), _ptr(va), kdt, B, N_cap, d, _ptr(ua), _ptr(ba), m, L, _ptr(tb),
+                                       _ptr(te), _ptr(kc), _ptr(vc), code, E_cap))
+    return kc, vc
 

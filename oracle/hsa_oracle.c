@@ -518,3 +518,76 @@ int orc_attn_v4_rows(int64_t n_rows, const void *q, int q_dt, const int64_t *row
     return err;
 }
 
+/* Learned, attention-like compression ([QbitAI] 混合注意力机制, CSA step 1: every m
+ * tokens' KV entries are merged into one by an attention-like mechanism with learned
+ * weights; the HCA paragraph: m' = 128 and, unlike CSA, no overlap).  The pages give
+ * no formula; reading: entry j pools the L tokens t_r = (j+1)*m - L + r, r = 0..L-1
+ * (L = 2m for CSA: the block and the one before it; L = m for HCA), dropping t_r < 0,
+ * with weights from a learned scoring vector u [d] and position bias bias [L]:
+ *     s_r = <u, K[b, t_r]> + bias[r],   a = softmax_r(s),
+ *     Kc[b, j] = sum_r a_r K[b, t_r],   Vc[b, j] = sum_r a_r V[b, t_r].
+ * Entry j still ends at token (j+1)*m - 1, so visibility E(p) is unchanged.  Blocks
+ * j in [tok_begin[b]/m, tok_end[b]/m) are written (out dtype f32/f64).
+ * Pinned by: u = 0, bias = 0, L = m gives the block mean (orc_compress with
+ * w = 1/m); a bias of -inf everywhere but r copies token t_r; adding a constant to
+ * bias changes nothing; L = 2m with the first m biases at -inf equals L = m. */
+int orc_compress_learned(const void *k, const void *v, int x_dt, int B, int64_t N_cap, int d,
+                         const double *u, const double *bias, int m, int L,
+                         const int64_t *tok_begin, const int64_t *tok_end,
+                         void *kc, void *vc, int out_dt, int64_t E_cap)
+{
+    if (B < 0 || d <= 0 || m <= 0 || L < 1 || (out_dt != ORC_F32 && out_dt != ORC_F64))
+        return ORC_ERR_ARG;
+    for (int b = 0; b < B; ++b) {
+        if (tok_begin[b] < 0 || tok_end[b] > N_cap || tok_begin[b] > tok_end[b])
+            return ORC_ERR_RANGE;
+        if (tok_end[b] / m > E_cap)
+            return ORC_ERR_RANGE;
+    }
+    int err = ORC_OK;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int b = 0; b < B; ++b) {
+        double *sc = (double *)malloc(sizeof(double) * (size_t)L);
+        if (!sc) {
+#pragma omp critical
+            err = ORC_ERR_NOMEM;
+            continue;
+        }
+        for (int64_t j = tok_begin[b] / m; j < tok_end[b] / m; ++j) {
+            int64_t t0 = (j + 1) * m - L;
+            double M = -INFINITY;
+            for (int r = 0; r < L; ++r) {
+                int64_t t = t0 + r;
+                sc[r] = -INFINITY;
+                if (t < 0)
+                    continue;
+                double dot = 0.0;
+                for (int c = 0; c < d; ++c)
+                    dot += u[c] * orc_load(k, x_dt, ((int64_t)b * N_cap + t) * d + c);
+                sc[r] = dot + bias[r];
+                if (sc[r] > M)
+                    M = sc[r];
+            }
+            double Z = 0.0;
+            for (int r = 0; r < L; ++r)
+                if (sc[r] != -INFINITY)
+                    Z += exp(sc[r] - M);
+            for (int c = 0; c < d; ++c) {
+                double ak = 0.0, av = 0.0;
+                for (int r = 0; r < L; ++r) {
+                    if (sc[r] == -INFINITY)
+                        continue;
+                    double a = exp(sc[r] - M) / Z;
+                    int64_t t = t0 + r;
+                    ak += a * orc_load(k, x_dt, ((int64_t)b * N_cap + t) * d + c);
+                    av += a * orc_load(v, x_dt, ((int64_t)b * N_cap + t) * d + c);
+                }
+                orc_store(kc, out_dt, ((int64_t)b * E_cap + j) * d + c, ak);
+                orc_store(vc, out_dt, ((int64_t)b * E_cap + j) * d + c, av);
+            }
+        }
+        free(sc);
+    }
+    return err;
+}
+

@@ -530,3 +530,67 @@ def test_v4_sink_weight_closed_form_and_limit():
     o3, l3 = oracle.attn_v4_rows(q[0], [0], [p], ent, m, np.full((1, 1), -1, np.int32), raw, 0, 0.5, gq, gk,
                                  1e-6, 8, 10000.0, z)
     assert not o3.any() and np.allclose(l3[0], z)
+
+
+# ------------------------------------------------- learned compressor ---
+# (QbitAI article, hybrid attention: CSA step 1 -- attention-like merge with learned
+# weights -- and the HCA paragraph -- no overlap; window/score reading in hsa_oracle.c)
+
+def _kv(seed, B=2, N=40, d=8):
+    g = np.random.default_rng(seed)
+    return g.standard_normal((B, N, d)), g.standard_normal((B, N, d)), g.standard_normal(d)
+
+
+def test_learned_zero_scores_is_block_mean():
+    k, v, _ = _kv(1)
+    m = 4
+    kc, vc = oracle.compress_learned(k, v, np.zeros(8), np.zeros(m), m, m, [0, 4], [40, 37], 10)
+    rk = oracle.compress(k, np.full(m, 1.0 / m), m, [0, 4], [40, 37], 10)
+    rv = oracle.compress(v, np.full(m, 1.0 / m), m, [0, 4], [40, 37], 10)
+    np.testing.assert_allclose(kc, rk, atol=1e-14)
+    np.testing.assert_allclose(vc, rv, atol=1e-14)
+
+
+@pytest.mark.parametrize("r", [0, 3, 5, 7])
+def test_learned_one_open_bias_copies_that_token(r):
+    k, v, u = _kv(2)
+    m, L = 4, 8
+    bias = np.full(L, -np.inf)
+    bias[r] = 0.0
+    kc, vc = oracle.compress_learned(k, v, u, bias, m, L, [8, 8], [40, 40], 10)
+    for j in range(2, 10):
+        t = (j + 1) * m - L + r
+        np.testing.assert_array_equal(kc[:, j], k[:, t])
+        np.testing.assert_array_equal(vc[:, j], v[:, t])
+
+
+def test_learned_bias_shift_and_masked_overlap():
+    k, v, u = _kv(3)
+    m = 4
+    bias = np.random.default_rng(4).standard_normal(2 * m)
+    a = oracle.compress_learned(k, v, u, bias, m, 2 * m, [0, 0], [40, 40], 10)
+    b = oracle.compress_learned(k, v, u, bias + 3.7, m, 2 * m, [0, 0], [40, 40], 10)
+    np.testing.assert_allclose(a[0], b[0], atol=1e-12)
+    np.testing.assert_allclose(a[1], b[1], atol=1e-12)
+    # the earlier block masked out: the same as no overlap
+    masked = np.concatenate([np.full(m, -np.inf), bias[m:]])
+    c = oracle.compress_learned(k, v, u, masked, m, 2 * m, [0, 0], [40, 40], 10)
+    d = oracle.compress_learned(k, v, u, bias[m:], m, m, [0, 0], [40, 40], 10)
+    np.testing.assert_allclose(c[0], d[0], atol=1e-14)
+    np.testing.assert_allclose(c[1], d[1], atol=1e-14)
+
+
+def test_learned_weights_follow_scores():
+    """two-token window, closed form: a_1 = sigmoid(s_1 - s_0)"""
+    k, v, u = _kv(5, B=1, N=12, d=6)
+    m, L = 1, 2
+    bias = np.array([0.2, -0.5])
+    kc, vc = oracle.compress_learned(k, v, u, bias, m, L, [1], [12], 12)
+    for j in range(1, 12):
+        s0, s1 = u @ k[0, j - 1] + bias[0], u @ k[0, j] + bias[1]
+        a1 = 1.0 / (1.0 + np.exp(s0 - s1))
+        np.testing.assert_allclose(kc[0, j], (1 - a1) * k[0, j - 1] + a1 * k[0, j], atol=1e-12)
+        np.testing.assert_allclose(vc[0, j], (1 - a1) * v[0, j - 1] + a1 * v[0, j], atol=1e-12)
+    # entry 0 has only token 0 in range
+    kc0, _ = oracle.compress_learned(k, v, u, bias, m, L, [0], [1], 12)
+    np.testing.assert_allclose(kc0[0, 0], k[0, 0], atol=1e-15)
