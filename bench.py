@@ -584,6 +584,12 @@ def run_prefill(dev, reps: int):
         out = torch.empty((B, T, H, d), dtype=torch.bfloat16, device=dev)
         r = {"workload": wl.name}
         r["compress_chunk_ms"] = timed(lambda: L.hsa_compress(kr, vr, pos0, full, T // m, w, m, kc, vc))
+        # the learned attention-like compressor (window 2m for CSA, m for HCA) on the same chunk
+        Lw = 2 * m if wl.kind == "csa" else m
+        u_l = torch.randn((d,), generator=g, device=dev) / d ** 0.5
+        b_l = torch.randn((Lw,), generator=g, device=dev)
+        r["compress_learned_chunk_ms"] = timed(lambda: L.hsa_compress_learned(kr, vr, pos0, full, T // m, u_l, b_l, m,
+                                                                              kc, vc))
         idx = cnt = None
         if wl.kind == "csa":
             qi = torch.randint(-127, 128, (B, T, wl.DI), generator=g, device=dev, dtype=torch.int16).to(torch.int8)

@@ -22,7 +22,7 @@ _STATUS = {0: "HSA_OK", 1: "HSA_ERR_INVALID_ARG", 2: "HSA_ERR_UNSUPPORTED", 3: "
            4: "HSA_ERR_CUDA", 5: "HSA_ERR_DEVICE_FLAG"}
 
 # every symbol include/hsa.h declares
-EXPORTS = ["hsa_last_error", "hsa_version", "hsa_check", "hsa_compress", "hsa_compress_append", "hsa_index_topk_workspace_size",
+EXPORTS = ["hsa_last_error", "hsa_version", "hsa_check", "hsa_compress", "hsa_compress_append", "hsa_compress_learned", "hsa_index_topk_workspace_size",
            "hsa_index_topk", "hsa_index_topk_noalloc", "hsa_attn_decode_workspace_size", "hsa_attn_decode",
            "hsa_attn_prefill_workspace_size", "hsa_attn_prefill", "hsa_index_scores", "hsa_topk_merge",
            "hsa_lse_merge", "hsa_rmsnorm_rope", "hsa_attn_finalize"]
@@ -47,6 +47,8 @@ def _load():
     lib.hsa_check.argtypes = [P]
     lib.hsa_compress.restype = I
     lib.hsa_compress.argtypes = [P, P, I, I, I, I64, I64, I64, P, P, I64, P, I, P, P, I64, I64, I64, P]
+    lib.hsa_compress_learned.restype = I
+    lib.hsa_compress_learned.argtypes = [P, P, I, I, I, I64, I64, I64, P, P, I64, P, P, I, I, P, P, I64, I64, I64, P]
     lib.hsa_compress_append.restype = I
     lib.hsa_compress_append.argtypes = [P, P, I, I, I, I, I64, I64, P, P, I, P, P, I64, P, P, I64, I64, I64, P]
     lib.hsa_index_topk_workspace_size.restype = I
@@ -115,6 +117,15 @@ def hsa_compress(k, v, tok_begin, tok_end, max_blocks, w, m, kc, vc, stream=None
     _chk(lib.hsa_compress(_p(k), _p(v), _dt(k), B, d, k.stride(0), k.stride(1), N_cap, _p(tok_begin), _p(tok_end),
                           int(max_blocks), _p(w), int(m), _p(kc), _p(vc), kc.stride(0), kc.stride(1), kc.shape[1],
                           _stream(stream)))
+
+
+def hsa_compress_learned(k, v, tok_begin, tok_end, max_blocks, u, bias, m, kc, vc, stream=None):
+    """Learned attention-like compression: window L = bias.numel() tokens ending at each block's last token."""
+    B, N_cap, d = k.shape
+    assert v.shape == k.shape and v.stride() == k.stride() and kc.stride() == vc.stride()
+    _chk(lib.hsa_compress_learned(_p(k), _p(v), _dt(k), B, d, k.stride(0), k.stride(1), N_cap, _p(tok_begin),
+                                  _p(tok_end), int(max_blocks), _p(u), _p(bias), int(m), int(bias.numel()), _p(kc),
+                                  _p(vc), kc.stride(0), kc.stride(1), kc.shape[1], _stream(stream)))
 
 
 def hsa_compress_append(k_new, v_new, pos0, w, m, state_k, state_v, kc, vc, stream=None):

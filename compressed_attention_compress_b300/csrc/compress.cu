@@ -12,6 +12,11 @@
 
 namespace hsa {
 
+__device__ __forceinline__ float load_elem(const float *p) { return *p; }
+__device__ __forceinline__ float load_elem(const __nv_bfloat16 *p) { return __bfloat162float(*p); }
+__device__ __forceinline__ void store_elem(float *p, float v) { *p = v; }
+__device__ __forceinline__ void store_elem(__nv_bfloat16 *p, float v) { *p = __float2bfloat16_rn(v); }
+
 template <typename T, int U>
 __global__ void __launch_bounds__(256) compress_kernel(CompressArgs a) {
     constexpr int V = ElemTraits<T>::kVec;
@@ -198,6 +203,106 @@ cudaError_t launch_compress_append(const CompressAppendArgs &a, bool bf16, cudaS
         compress_append_kernel<__nv_bfloat16><<<grid, 128, 0, s>>>(a);
     else
         compress_append_kernel<float><<<grid, 128, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+// ------------------------------------------------------ learned compression
+// Attention-like pooling with learned weights (QbitAI article, 混合注意力机制: CSA step 1
+// merges every m tokens "through an attention-like mechanism with learned weights";
+// HCA has no overlap).  Entry j pools the L tokens t_r = (j+1)*m - L + r (t_r >= 0)
+// with a = softmax_r(<u, K[t_r]> + bias[r]); the same weights pool K and V.  One warp
+// per entry: lanes score the window's tokens (one token row per lane), the warp
+// takes the softmax, then every lane accumulates its d/32 channels over the window.
+template <typename T>
+__global__ void __launch_bounds__(128) compress_learned_kernel(CompressLearnedArgs a) {
+    extern __shared__ float s_dyn[];
+    float *s_u = s_dyn;                        // [d]
+    float *s_sc = s_dyn + a.d + (threadIdx.x >> 5) * a.L;  // [4][L]
+    for (int c = threadIdx.x; c < a.d; c += blockDim.x) s_u[c] = a.u[c];
+    __syncthreads();
+    const int lane = threadIdx.x & 31;
+    const int64_t item = (int64_t)blockIdx.x * 4 + (threadIdx.x >> 5);
+    if (item >= (int64_t)a.B * a.max_blocks) return;
+    const int b = (int)(item / a.max_blocks);
+    const int64_t j = a.tok_begin[b] / a.m + (item - (int64_t)b * a.max_blocks);
+    if (j >= a.tok_end[b] / a.m) return;
+    if (a.tok_begin[b] < 0 || (j + 1) * a.m > a.N_cap || j >= a.E_cap) {
+        if (lane == 0) raise_flag(FLAG_COMPRESS_RANGE);
+        return;
+    }
+    const T *kb = static_cast<const T *>(a.k) + b * a.in_sb;
+    const T *vb = static_cast<const T *>(a.v) + b * a.in_sb;
+    const int64_t t0 = (j + 1) * a.m - a.L;
+    // scores, one window token per lane
+    for (int r = lane; r < a.L; r += 32) {
+        const int64_t t = t0 + r;
+        float sc = -INFINITY;
+        if (t >= 0) {
+            // the token row in 16-byte vectors (rows are 16-byte aligned)
+            constexpr int V = ElemTraits<T>::kVec;
+            const char *row = reinterpret_cast<const char *>(kb + t * a.in_st);
+            float dot = 0.f;
+            for (int c = 0; c < a.d; c += V) {
+                const int4 x = ld_nc_v4(row + c * sizeof(T));
+                const uint32_t *xp = reinterpret_cast<const uint32_t *>(&x);
+                if constexpr (V == 8) {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        dot = fmaf(s_u[c + 2 * e], bf16_lo(xp[e]), dot);
+                        dot = fmaf(s_u[c + 2 * e + 1], bf16_hi(xp[e]), dot);
+                    }
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) dot = fmaf(s_u[c + e], __uint_as_float(xp[e]), dot);
+                }
+            }
+            sc = dot + a.bias[r];
+        }
+        s_sc[r] = sc;
+    }
+    __syncwarp();
+    float M = -INFINITY;
+    for (int r = lane; r < a.L; r += 32) M = fmaxf(M, s_sc[r]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    float Z = 0.f;
+    for (int r = lane; r < a.L; r += 32) Z += s_sc[r] == -INFINITY ? 0.f : expf(s_sc[r] - M);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) Z += __shfl_xor_sync(0xffffffffu, Z, o);
+    const float invZ = 1.f / Z;
+    // weighted sums over the window, d / 32 channels per lane
+    const int per = a.d / 32, c0 = lane * per;
+    float ak[16], av[16];
+    for (int e = 0; e < per; ++e) ak[e] = av[e] = 0.f;
+    for (int r = 0; r < a.L; ++r) {
+        const float sc = s_sc[r];
+        if (sc == -INFINITY) continue;  // uniform across the warp
+        const float w = expf(sc - M) * invZ;
+        const int64_t t = t0 + r;
+        const T *kr = kb + t * a.in_st + c0;
+        const T *vr = vb + t * a.in_st + c0;
+        for (int e = 0; e < per; ++e) {
+            ak[e] = fmaf(w, load_elem(kr + e), ak[e]);
+            av[e] = fmaf(w, load_elem(vr + e), av[e]);
+        }
+    }
+    T *ko = static_cast<T *>(a.kc) + b * a.out_sb + j * a.out_se + c0;
+    T *vo = static_cast<T *>(a.vc) + b * a.out_sb + j * a.out_se + c0;
+    for (int e = 0; e < per; ++e) {
+        store_elem(ko + e, ak[e]);
+        store_elem(vo + e, av[e]);
+    }
+}
+
+cudaError_t launch_compress_learned(const CompressLearnedArgs &a, bool bf16, cudaStream_t s) {
+    const int64_t items = (int64_t)a.B * a.max_blocks;
+    if (items <= 0) return cudaSuccess;
+    const size_t smem = sizeof(float) * ((size_t)a.d + 4 * (size_t)a.L);
+    const unsigned grid = (unsigned)((items + 3) / 4);
+    if (bf16)
+        compress_learned_kernel<__nv_bfloat16><<<grid, 128, smem, s>>>(a);
+    else
+        compress_learned_kernel<float><<<grid, 128, smem, s>>>(a);
     return cudaGetLastError();
 }
 

@@ -195,6 +195,31 @@ hsa_status_t hsa_compress(const void *k, const void *v, hsa_dtype_t dt, int B, i
                     "compress");
 }
 
+hsa_status_t hsa_compress_learned(const void *k, const void *v, hsa_dtype_t dt, int B, int d, int64_t in_sb,
+                                  int64_t in_st, int64_t N_cap, const int64_t *tok_begin, const int64_t *tok_end,
+                                  int64_t max_blocks, const float *u, const float *bias, int m, int L, void *kc,
+                                  void *vc, int64_t out_sb, int64_t out_se, int64_t E_cap, hsa_stream_t stream) {
+    if (!dtype_ok(dt)) return fail(HSA_ERR_UNSUPPORTED, "dtype %d", (int)dt);
+    if (B < 0 || d <= 0 || m <= 0 || L < 1 || max_blocks < 0 || N_cap < 0 || E_cap < 0)
+        return fail(HSA_ERR_INVALID_ARG, "bad size (B=%d d=%d m=%d L=%d)", B, d, m, L);
+    if (L > 1024 || m > 4096) return fail(HSA_ERR_UNSUPPORTED, "L above 1024 or m above 4096");
+    if (d % 32 || d > 512) return fail(HSA_ERR_UNSUPPORTED, "d must be a multiple of 32 up to 512");
+    if (B == 0 || max_blocks == 0) return ok();
+    if (!k || !v || !kc || !vc || !tok_begin || !tok_end || !u || !bias) return fail(HSA_ERR_INVALID_ARG, "null pointer");
+    if (in_st < d || out_se < d) return fail(HSA_ERR_INVALID_ARG, "row strides overlap rows");
+    const int64_t vec = 16 / (int64_t)esize(dt);
+    if (!aligned16(k) || !aligned16(v) || in_sb % vec || in_st % vec)
+        return fail(HSA_ERR_UNSUPPORTED, "k, v and their strides must be 16-byte aligned");
+    DevInfo di;
+    hsa_status_t st = device_info(di);
+    if (st != HSA_OK) return st;
+    if ((st = pending_error()) != HSA_OK) return st;
+    hsa::CompressLearnedArgs a{k, v, B, d, in_sb, in_st, N_cap, tok_begin, tok_end, max_blocks, u, bias, m, L,
+                               kc, vc, out_sb, out_se, E_cap};
+    return launched(hsa::launch_compress_learned(a, dt == HSA_BF16, reinterpret_cast<cudaStream_t>(stream)),
+                    "compress_learned");
+}
+
 hsa_status_t hsa_compress_append(const void *k_new, const void *v_new, hsa_dtype_t dt, int B, int T, int d,
                                  int64_t new_sb, int64_t new_st, const int64_t *pos0, const float *w, int m,
                                  float *state_k, float *state_v, int64_t state_sb, void *kc, void *vc, int64_t out_sb,

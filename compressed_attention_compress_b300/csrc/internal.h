@@ -32,6 +32,19 @@ struct CompressAppendArgs {
     int64_t out_sb, out_se, E_cap;
 };
 cudaError_t launch_compress_append(const CompressAppendArgs &a, bool bf16, cudaStream_t s);
+struct CompressLearnedArgs {
+    const void *k, *v;
+    int B, d;
+    int64_t in_sb, in_st, N_cap;
+    const int64_t *tok_begin, *tok_end;
+    int64_t max_blocks;
+    const float *u;      // [d]
+    const float *bias;   // [L]
+    int m, L;
+    void *kc, *vc;
+    int64_t out_sb, out_se, E_cap;
+};
+cudaError_t launch_compress_learned(const CompressLearnedArgs &a, bool bf16, cudaStream_t s);
 
 // ---------------------------------------------------------------- indexer
 struct IndexArgs {

@@ -109,6 +109,27 @@ HSA_API hsa_status_t hsa_compress(const void *k, const void *v, hsa_dtype_t dt, 
                           hsa_stream_t stream);
 
 /*
+ * hsa_compress_learned -- attention-like compression with learned weights
+ * (QbitAI article, 混合注意力机制: CSA step 1 merges every m tokens "through an
+ * attention-like mechanism with learned weights"; the HCA paragraph: m' = 128
+ * and no overlap, unlike CSA).  The pages give no formula; this library reads
+ * it as: entry j pools the L tokens t_r = (j+1)*m - L + r, r = 0..L-1
+ * (t_r >= 0; L = 2m for CSA, the block and the one before it; L = m for HCA):
+ *   s_r = <u, k[b, t_r]> + bias[r],  a = softmax_r(s)  (fp32),
+ *   kc[b, j] = sum_r a_r k[b, t_r],   vc[b, j] = sum_r a_r v[b, t_r]
+ * rounded once to `dt`, for blocks j in [tok_begin[b] / m, tok_end[b] / m).
+ * Entry j still ends at token (j+1)*m - 1, so visibility is unchanged.
+ *   u          device fp32 [d];  bias  device fp32 [L]
+ * Other arguments as hsa_compress; d a multiple of 32 up to 512, 1 <= L <= 1024.
+ */
+HSA_API hsa_status_t hsa_compress_learned(const void *k, const void *v, hsa_dtype_t dt, int B, int d,
+                                          int64_t in_sb, int64_t in_st, int64_t N_cap,
+                                          const int64_t *tok_begin, const int64_t *tok_end, int64_t max_blocks,
+                                          const float *u, const float *bias, int m, int L,
+                                          void *kc, void *vc, int64_t out_sb, int64_t out_se, int64_t E_cap,
+                                          hsa_stream_t stream);
+
+/*
  * hsa_compress_append -- decode-time compression with a partial-block state
  * cache, the incremental form of hsa_compress (the yage.ai essay
  * "deepseek-v4-agentic-workload", paragraph on what hybrid attention costs:
