@@ -1,0 +1,509 @@
+// Prefill attention over each query token's own selected entries plus its window
+// (CSA layer) on the 5th-generation tensor cores.
+//
+// QbitAI article "DeepSeek V4报告太详尽了！", section 混合注意力机制: CSA step 3 runs
+// Multi-Query Attention over the top-k compressed entries the indexer selected for
+// the query token; the sliding-window paragraph adds the most recent raw tokens to
+// the same softmax.
+//
+// Every query token has its own item set, shared by its H = 64 heads, so a token is
+// an M = 64 (heads) problem: S = Q K_j^T (N = 128 items per tile, K = d = 128) and
+// O += P V_j, with S and O in TMEM (row h of an M = 64 accumulator lives in TMEM
+// lane (h / 16) * 32 + h % 16).  One persistent CTA per SM walks tokens:
+//   warps 0-3  softmax, one head per thread (lanes 0-15 of each warp): S from TMEM,
+//              masked maximum, exponents, P (bf16) into shared memory for the
+//              second MMA, O rescaled in TMEM only when the maximum grows by > 2^8.
+//   warps 4-7  gather: each thread resolves one item row of tile j (selected entry
+//              of Kc/Vc or window token of the raw cache, zero-filled when
+//              invalid); half-warps then copy whole 256-byte rows with 16-byte
+//              cp.async into a 5-slot ring of 32 KiB 128-byte-swizzled tiles; a
+//              128-bit validity mask per tile goes to a small ring of its own.
+//              Thread 0 of the group also loads each token's Q by TMA.
+//   warp 8     MMA issuer (one thread): S(g) into one of two TMEM buffers, then
+//              O += P(g-1) V(g-1); completion via tcgen05.commit.
+// All waits are bounded; a wait that gives up raises the device flag and the CTA
+// stops issuing work.
+#include <math.h>
+
+#include <cudaTypedefs.h>
+
+#include "internal.h"
+#include "tc_common.cuh"
+
+namespace hsa {
+
+namespace {
+
+constexpr int kH = 64;        // heads = MMA M
+constexpr int kD = 128;       // head dim
+constexpr int kN = 128;       // items per tile
+constexpr int kQBytes = kH * kD * 2;       // 16 KiB
+constexpr int kQBlk = kH * 128;            // 8 KiB per 64-column block of Q or P
+constexpr int kTile = kN * kD * 2;         // 32 KiB K or V tile
+constexpr int kTBlk = kN * 128;            // 16 KiB per 64-column block of a tile
+constexpr int kRing = 5;
+constexpr int kMaskRing = 8;
+constexpr int kSoftWarps = 4, kGatherWarps = 4;
+constexpr int kThreads = (kSoftWarps + kGatherWarps + 1) * 32;
+constexpr int kGatherThreads = kGatherWarps * 32;
+constexpr int kLag = 3;       // cp.async groups a gather thread keeps in flight: the MMA takes
+                              // K_{g+1} before releasing V_g, so kLag <= kRing - 2 keeps the ring live
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescale = 8.0f;
+constexpr unsigned long long kWaitLimit = 1ull << 24;
+
+struct __align__(8) Bars {
+    uint64_t q_full[2], q_empty[2];
+    uint64_t kv_full[kRing], kv_empty[kRing];
+    uint64_t m_full[kMaskRing], m_empty[kMaskRing];
+    uint64_t s_full[2], s_free[2];
+    uint64_t p_full, o_done, o_free, mma_fin;
+};
+
+struct GatherArgs {
+    int rows, T, topk, window, m, n_tiles;
+    int64_t E_cap, N_cap, c_sb, c_se, r_sb, r_st;
+    const int64_t *q_pos0;
+    const int32_t *idx, *cnt;
+    const __nv_bfloat16 *kc, *vc, *k_raw, *v_raw;
+    float scale_log2;
+    __nv_bfloat16 *out;
+    float *lse;
+};
+
+__device__ __forceinline__ bool wait_bar(uint64_t *bar, unsigned parity, volatile int *abort) {
+    for (unsigned long long i = 0; i < kWaitLimit; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 255) == 255 && *abort) return false;
+    }
+    raise_flag(FLAG_ATTN_RANGE | 0x800u);
+    *abort = 1;
+    return false;
+}
+__device__ __forceinline__ void arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ uint64_t fma_f32x2(uint64_t x, uint64_t y, uint64_t z) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;\n" : "=l"(d) : "l"(x), "l"(y), "l"(z));
+    return d;
+}
+__device__ __forceinline__ uint64_t add_f32x2(uint64_t x, uint64_t y) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;\n" : "=l"(d) : "l"(x), "l"(y));
+    return d;
+}
+__device__ __forceinline__ uint64_t pack2(float lo, float hi) {
+    return ((uint64_t)__float_as_uint(hi) << 32) | __float_as_uint(lo);
+}
+__device__ __forceinline__ float lo_of(uint64_t v) { return __uint_as_float((uint32_t)v); }
+__device__ __forceinline__ float hi_of(uint64_t v) { return __uint_as_float((uint32_t)(v >> 32)); }
+template <int N>
+__device__ __forceinline__ void cp_wait() {
+    asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_gather_tc_kernel(const __grid_constant__ CUtensorMap tm_q, GatherArgs a) {
+    extern __shared__ __align__(16) unsigned char smem_raw[];  // rounded up to 1024 at run time
+    unsigned char *smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+    unsigned char *sQ = smem;                          // 2 x 16 KiB
+    unsigned char *sRing = smem + 2 * kQBytes;         // kRing x 32 KiB
+    unsigned char *sP = sRing + kRing * kTile;         // 16 KiB
+    __shared__ Bars bars;
+    __shared__ uint32_t s_mask[kMaskRing][4];
+    __shared__ uint32_t s_tmem;
+    __shared__ int s_abort;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bars.q_full[i], 1);
+            mbar_init(&bars.q_empty[i], 1);
+            mbar_init(&bars.s_full[i], 1);
+            mbar_init(&bars.s_free[i], kSoftWarps * 32);
+        }
+        for (int i = 0; i < kRing; ++i) {
+            mbar_init(&bars.kv_full[i], kGatherThreads);
+            mbar_init(&bars.kv_empty[i], 1);
+        }
+        for (int i = 0; i < kMaskRing; ++i) {
+            mbar_init(&bars.m_full[i], kGatherWarps);
+            mbar_init(&bars.m_empty[i], kSoftWarps * 32);
+        }
+        mbar_init(&bars.p_full, kSoftWarps * 32);
+        mbar_init(&bars.o_done, 1);
+        mbar_init(&bars.o_free, kSoftWarps * 32);
+        mbar_init(&bars.mma_fin, 1);
+        fence_mbar_init();
+        s_abort = 0;
+    }
+    if (warp == 0) tc::tmem_alloc(&s_tmem, 512);
+    tc::fence_before();
+    __syncthreads();
+    tc::fence_after();
+    const uint32_t tmem = s_tmem;
+    const uint32_t tS[2] = {tmem, tmem + 128};
+    const uint32_t tO = tmem + 256;
+    const int nt = a.n_tiles;
+
+    if (warp >= kSoftWarps && warp < kSoftWarps + kGatherWarps) {
+        // ---------------------------------------------------------------- gather
+        const int gt = threadIdx.x - kSoftWarps * 32;  // 0..127: the item row this thread copies
+        const int gw = gt >> 5;
+        int it = 0;
+        int64_t u = 0;  // tiles (K or V) issued
+        int64_t g = 0;  // item tiles (mask ring uses)
+        bool ok = true;
+        for (int row = blockIdx.x; row < a.rows && ok; row += gridDim.x, ++it) {
+            const int b = row / a.T, t = row - (row / a.T) * a.T;
+            const int64_t p = a.q_pos0[b] + t;
+            int64_t E = num_entries(p, a.m);
+            if (E > a.E_cap) E = a.E_cap;
+            const int cntr = a.cnt ? min(max(a.cnt[row], 0), a.topk) : a.topk;
+            if (gt == 0) {
+                if (it >= 2) ok = wait_bar(&bars.q_empty[it & 1], (unsigned)(((it >> 1) - 1) & 1), &s_abort);
+                if (ok) {
+                    mbar_expect_tx(&bars.q_full[it & 1], kQBytes);
+                    tc::tma_load_2d(sQ + (it & 1) * kQBytes, &tm_q, 0, row * kH, &bars.q_full[it & 1]);
+                    tc::tma_load_2d(sQ + (it & 1) * kQBytes + kQBlk, &tm_q, 64, row * kH, &bars.q_full[it & 1]);
+                }
+            }
+            ok = __all_sync(0xffffffffu, ok);  // the warp's lanes leave together (ballots below)
+            for (int j = 0; j < nt && ok; ++j, ++g) {
+                // the item this thread copies, and whether it is valid
+                const int slot_i = j * kN + gt;
+                const __nv_bfloat16 *ksrc = nullptr, *vsrc = nullptr;
+                if (slot_i < a.topk) {
+                    const int32_t e = slot_i < cntr ? a.idx[(int64_t)row * a.topk + slot_i] : -1;
+                    if (e >= E) raise_flag(FLAG_ATTN_INDEX);
+                    if (e >= 0 && e < E) {
+                        ksrc = a.kc + b * a.c_sb + (int64_t)e * a.c_se;
+                        vsrc = a.vc + b * a.c_sb + (int64_t)e * a.c_se;
+                    }
+                } else if (slot_i < a.topk + a.window) {
+                    const int64_t tr = p - a.window + 1 + (slot_i - a.topk);
+                    if (tr >= 0 && tr <= p) {
+                        if (tr >= a.N_cap) raise_flag(FLAG_ATTN_RANGE);
+                        else {
+                            ksrc = a.k_raw + b * a.r_sb + tr * a.r_st;
+                            vsrc = a.v_raw + b * a.r_sb + tr * a.r_st;
+                        }
+                    }
+                }
+                // validity mask of the tile (one word per gather warp)
+                const uint32_t bits = __ballot_sync(0xffffffffu, ksrc != nullptr);
+                const int ms = (int)(g % kMaskRing);
+                if (g >= kMaskRing)
+                    ok = wait_bar(&bars.m_empty[ms], (unsigned)(((g / kMaskRing) - 1) & 1), &s_abort);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+                if (lane == 0) {
+                    s_mask[ms][gw] = bits;
+                    arrive(&bars.m_full[ms]);
+                }
+                for (int kv = 0; kv < 2 && ok; ++kv, ++u) {
+                    const int slot = (int)(u % kRing);
+                    if (u >= kRing) ok = wait_bar(&bars.kv_empty[slot], (unsigned)(((u / kRing) - 1) & 1), &s_abort);
+                    ok = __all_sync(0xffffffffu, ok);
+                    if (!ok) break;
+                    // a half-warp copies one 256-byte row (lane l: 16-byte chunk l % 16), so
+                    // each instruction moves two whole rows; row pointers come by shuffle
+                    // from the lane that resolved the row
+                    const __nv_bfloat16 *src = kv ? vsrc : ksrc;
+                    const unsigned long long sv = reinterpret_cast<unsigned long long>(src);
+                    unsigned char *dst = sRing + slot * kTile;
+                    const int c = lane & 15;
+#pragma unroll 4
+                    for (int i = 0; i < 16; ++i) {
+                        const int rl = 2 * i + (lane >> 4);            // row within this warp's 32
+                        const unsigned long long rs = __shfl_sync(0xffffffffu, sv, rl);
+                        const int r = gw * 32 + rl;                     // row within the tile
+                        const uint32_t off = (uint32_t)((c >> 3) * kTBlk + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+                        const __nv_bfloat16 *rp = reinterpret_cast<const __nv_bfloat16 *>(rs);
+                        cp_async_16(smem_u32(dst + off), rp ? (const void *)(rp + c * 8) : (const void *)a.kc,
+                                    rp ? 16 : 0);  // zero-fill invalid rows
+                    }
+                    cp_async_commit();
+                    // the tile issued kLag groups ago has landed: publish it to the MMA
+                    if (u >= kLag) {
+                        cp_wait<kLag>();
+                        tc::fence_proxy_async();
+                        arrive(&bars.kv_full[(u - kLag) % kRing]);
+                    }
+                }
+            }
+        }
+        // publish the last tiles (and let every copy land before the CTA exits)
+        cp_wait<0>();
+        tc::fence_proxy_async();
+        for (int64_t v = (u > kLag ? u - kLag : 0); v < u; ++v) arrive(&bars.kv_full[v % kRing]);
+        if (!ok) s_abort = 1;
+        if (gt == 0 && it > 0) {
+            volatile int never = 0;
+            wait_bar(&bars.q_full[(it - 1) & 1], (unsigned)(((it - 1) >> 1) & 1), &never);
+        }
+    } else if (warp == kSoftWarps + kGatherWarps) {
+        // ------------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idS = tc::idesc_bf16(kH, kN, false, false);
+            constexpr uint32_t idO = tc::idesc_bf16(kH, kD, false, true);
+            const uint32_t aP = smem_u32(sP);
+            int it = 0;
+            int64_t g = 0, u = 0;
+            bool ok = true;
+            auto wait_tile = [&](int64_t uu) -> uint32_t {
+                const int slot = (int)(uu % kRing);
+                ok = ok && wait_bar(&bars.kv_full[slot], (unsigned)((uu / kRing) & 1), &s_abort);
+                return smem_u32(sRing + slot * kTile);
+            };
+            auto issue_pv = [&](int64_t gg, int64_t uv, bool first) {
+                ok = ok && wait_bar(&bars.p_full, (unsigned)(gg & 1), &s_abort);
+                if (ok && first && it > 0) ok = wait_bar(&bars.o_free, (unsigned)((it - 1) & 1), &s_abort);
+                const uint32_t aV = wait_tile(uv);
+                if (!ok) return;
+                tc::fence_after();
+#pragma unroll
+                for (int kk = 0; kk < kN / 16; ++kk) {
+                    const uint64_t da = tc::desc_sw128(aP + (kk >> 2) * kQBlk + (kk & 3) * 32, 16, 1024);
+                    const uint64_t db = tc::desc_sw128(aV + kk * 16 * 128, kTBlk, 1024);
+                    tc::mma_bf16(tO, da, db, idO, (first && kk == 0) ? 0u : 1u);
+                }
+                tc::commit(&bars.o_done);
+                tc::commit(&bars.kv_empty[uv % kRing]);
+            };
+            for (int row = blockIdx.x; row < a.rows && ok; row += gridDim.x, ++it) {
+                ok = wait_bar(&bars.q_full[it & 1], (unsigned)((it >> 1) & 1), &s_abort);
+                if (!ok) break;
+                tc::fence_after();
+                const uint32_t aQ = smem_u32(sQ + (it & 1) * kQBytes);
+                int64_t uv_prev = -1;
+                for (int j = 0; j < nt && ok; ++j, ++g) {
+                    const int64_t uk = u, uv = u + 1;
+                    u += 2;
+                    const uint32_t aK = wait_tile(uk);
+                    if (ok && g >= 2) ok = wait_bar(&bars.s_free[g & 1], (unsigned)(((g >> 1) - 1) & 1), &s_abort);
+                    if (!ok) break;
+                    tc::fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < kD / 16; ++kk) {
+                        const uint64_t da = tc::desc_sw128(aQ + (kk >> 2) * kQBlk + (kk & 3) * 32, 16, 1024);
+                        const uint64_t db = tc::desc_sw128(aK + (kk >> 2) * kTBlk + (kk & 3) * 32, 16, 1024);
+                        tc::mma_bf16(tS[g & 1], da, db, idS, kk > 0 ? 1u : 0u);
+                    }
+                    tc::commit(&bars.s_full[g & 1]);
+                    tc::commit(&bars.kv_empty[uk % kRing]);
+                    if (j == nt - 1) tc::commit(&bars.q_empty[it & 1]);
+                    if (j > 0) issue_pv(g - 1, uv_prev, j == 1);
+                    uv_prev = uv;
+                }
+                if (ok) issue_pv(g - 1, uv_prev, nt == 1);
+            }
+            if (!ok) s_abort = 1;
+            tc::commit(&bars.mma_fin);
+            volatile int never = 0;
+            wait_bar(&bars.mma_fin, 0u, &never);
+        }
+    } else if (warp < kSoftWarps) {
+        // ---------------------------------------------------------------- softmax
+        const bool active = lane < 16;
+        const int h = warp * 16 + lane;  // head of this thread (active lanes)
+        const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+        int64_t g = 0;
+        int it = 0;
+        bool ok = true;
+        for (int row = blockIdx.x; row < a.rows && ok; row += gridDim.x, ++it) {
+            float m_used = -INFINITY, l = 0.f;
+            for (int j = 0; j < nt && ok; ++j, ++g) {
+                ok = wait_bar(&bars.s_full[g & 1], (unsigned)((g >> 1) & 1), &s_abort);
+                const int ms = (int)(g % kMaskRing);
+                if (ok) ok = wait_bar(&bars.m_full[ms], (unsigned)((g / kMaskRing) & 1), &s_abort);
+                ok = __all_sync(0xffffffffu, ok);  // warp-collective TMEM loads below
+                if (!ok) break;
+                tc::fence_after();
+                uint32_t mw[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) mw[q] = s_mask[ms][q];
+                arrive(&bars.m_empty[ms]);
+                // pass 1: masked raw maximum over S, 64 columns at a time (eight chains);
+                // tiles with every item valid (the common case) skip the mask
+                const bool all_valid = (mw[0] & mw[1] & mw[2] & mw[3]) == 0xffffffffu;
+                float mx8[8];
+#pragma unroll
+                for (int q = 0; q < 8; ++q) mx8[q] = -INFINITY;
+#pragma unroll
+                for (int hf = 0; hf < 2; ++hf) {
+                    uint32_t v[64];
+                    tc::tmem_ld32(tS[g & 1] + lane_off + hf * 64, v);
+                    tc::tmem_ld32(tS[g & 1] + lane_off + hf * 64 + 32, v + 32);
+                    tc::tmem_wait_ld();
+                    if (all_valid) {
+#pragma unroll
+                        for (int c = 0; c < 64; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], __uint_as_float(v[c]));
+                    } else {
+                        const uint32_t w0 = mw[2 * hf], w1 = mw[2 * hf + 1];
+#pragma unroll
+                        for (int c = 0; c < 64; ++c) {
+                            const bool ok_c = ((c < 32 ? w0 : w1) >> (c & 31)) & 1u;
+                            mx8[c & 7] = fmaxf(mx8[c & 7], ok_c ? __uint_as_float(v[c]) : -INFINITY);
+                        }
+                    }
+                }
+                const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                                       fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) *
+                                 a.scale_log2;
+                bool rescale = false;
+                float alpha = 1.f;
+                if (mx > m_used + kRescale) {
+                    if (m_used != -INFINITY) {
+                        alpha = tc::ex2(m_used - mx);
+                        rescale = j > 0;
+                    }
+                    l *= (m_used == -INFINITY) ? 0.f : alpha;
+                    m_used = mx;
+                }
+                // P and O are free once the previous PV has completed
+                if (g > 0) ok = wait_bar(&bars.o_done, (unsigned)((g - 1) & 1), &s_abort);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+                tc::fence_after();
+                if (__any_sync(0xffffffffu, rescale && active)) {
+#pragma unroll
+                    for (int c = 0; c < kD / 32; ++c) {
+                        uint32_t o[32];
+                        tc::tmem_ld32(tO + lane_off + c * 32, o);
+                        tc::tmem_wait_ld();
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                        tc::tmem_st32(tO + lane_off + c * 32, o);
+                    }
+                    tc::tmem_wait_st();
+                }
+                // pass 2: P = 2^(x * scale_log2 - m_used) in bf16, 128-byte-swizzled K-major rows;
+                // invalid items read as -inf (exponent 0), the scale goes into a packed FMA
+                const float nmu = m_used == -INFINITY ? 0.f : -m_used;
+                const uint64_t nmu2 = pack2(nmu, nmu), sc2 = pack2(a.scale_log2, a.scale_log2);
+                uint64_t acc2[4] = {0, 0, 0, 0};
+#pragma unroll
+                for (int hf = 0; hf < 2; ++hf) {
+                    uint32_t v[64];
+                    tc::tmem_ld32(tS[g & 1] + lane_off + hf * 64, v);
+                    tc::tmem_ld32(tS[g & 1] + lane_off + hf * 64 + 32, v + 32);
+                    tc::tmem_wait_ld();
+                    if (!all_valid) {
+                        const uint32_t w0 = mw[2 * hf], w1 = mw[2 * hf + 1];
+#pragma unroll
+                        for (int c = 0; c < 64; ++c)
+                            if (!(((c < 32 ? w0 : w1) >> (c & 31)) & 1u)) v[c] = __float_as_uint(-INFINITY);
+                    }
+                    if (active) {
+#pragma unroll
+                        for (int cc = 0; cc < 8; ++cc) {
+                            uint32_t pk[4];
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const int c0 = cc * 8 + 2 * e;
+                                const uint64_t arg = fma_f32x2(((uint64_t)v[c0 + 1] << 32) | v[c0], sc2, nmu2);
+                                const float p0 = tc::ex2(lo_of(arg)), p1 = tc::ex2(hi_of(arg));
+                                acc2[e] = add_f32x2(acc2[e], pack2(p0, p1));
+                                pk[e] = pack_bf16x2(p0, p1);
+                            }
+                            *reinterpret_cast<uint4 *>(sP + hf * kQBlk + h * 128 + ((cc ^ (h & 7)) << 4)) =
+                                make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                        }
+                    }
+                }
+                const uint64_t s4 = add_f32x2(add_f32x2(acc2[0], acc2[1]), add_f32x2(acc2[2], acc2[3]));
+                const float sum = lo_of(s4) + hi_of(s4);
+                tc::fence_before();
+                arrive(&bars.s_free[g & 1]);  // S has been read in full
+                l += sum;
+                tc::fence_proxy_async();
+                tc::fence_before();
+                arrive(&bars.p_full);
+            }
+            if (!ok) break;
+            // epilogue: O / l once the token's last PV is done
+            ok = wait_bar(&bars.o_done, (unsigned)((g - 1) & 1), &s_abort);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            tc::fence_after();
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+            __nv_bfloat16 *orow = a.out + ((int64_t)row * kH + h) * kD;
+#pragma unroll
+            for (int c = 0; c < kD / 32; ++c) {
+                uint32_t o[32];
+                tc::tmem_ld32(tO + lane_off + c * 32, o);
+                tc::tmem_wait_ld();
+                if (active) {
+#pragma unroll
+                    for (int e = 0; e < 32; e += 8) {
+                        uint4 pk;
+                        pk.x = pack_bf16x2(__uint_as_float(o[e]) * inv, __uint_as_float(o[e + 1]) * inv);
+                        pk.y = pack_bf16x2(__uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv);
+                        pk.z = pack_bf16x2(__uint_as_float(o[e + 4]) * inv, __uint_as_float(o[e + 5]) * inv);
+                        pk.w = pack_bf16x2(__uint_as_float(o[e + 6]) * inv, __uint_as_float(o[e + 7]) * inv);
+                        *reinterpret_cast<uint4 *>(orow + c * 32 + e) = pk;
+                    }
+                }
+            }
+            tc::fence_before();
+            arrive(&bars.o_free);
+            if (active && a.lse) a.lse[(int64_t)row * kH + h] = l > 0.f ? (m_used + log2f(l)) * kLn2 : -INFINITY;
+        }
+        if (!ok) s_abort = 1;
+    }
+    tc::fence_before();
+    __syncthreads();
+    tc::fence_after();
+    if (warp == 0) tc::tmem_dealloc(tmem, 512);
+}
+
+constexpr size_t kSmemBytes = 1024 + 2 * (size_t)kQBytes + kRing * (size_t)kTile + kQBytes;
+
+}  // namespace
+
+bool gather_tc_supported(const AttnArgs &a) {
+    return a.d == kD && a.H == kH && a.idx != nullptr && a.topk > 0 && a.rows > 0;
+}
+
+cudaError_t launch_attn_gather_tc(const AttnArgs &a, int num_sms, cudaStream_t s) {
+    CUtensorMap tq;
+    {
+        const uint64_t dims[2] = {(uint64_t)kD, (uint64_t)a.rows * kH};
+        const uint64_t str[1] = {(uint64_t)kD};
+        if (!make_tmap_bf16(&tq, a.q, 2, dims, str, kH)) return cudaErrorInvalidValue;
+    }
+    GatherArgs g;
+    g.rows = a.rows;
+    g.T = a.T;
+    g.topk = a.topk;
+    g.window = a.window;
+    g.m = a.m;
+    g.n_tiles = (a.topk + a.window + kN - 1) / kN;
+    g.E_cap = a.E_cap;
+    g.N_cap = a.N_cap;
+    g.c_sb = a.c_sb;
+    g.c_se = a.c_se;
+    g.r_sb = a.r_sb;
+    g.r_st = a.r_st;
+    g.q_pos0 = a.pos;
+    g.idx = a.idx;
+    g.cnt = a.cnt;
+    g.kc = static_cast<const __nv_bfloat16 *>(a.kc);
+    g.vc = static_cast<const __nv_bfloat16 *>(a.vc);
+    g.k_raw = static_cast<const __nv_bfloat16 *>(a.k_raw);
+    g.v_raw = static_cast<const __nv_bfloat16 *>(a.v_raw);
+    g.scale_log2 = a.scale * kLog2e;
+    g.out = static_cast<__nv_bfloat16 *>(a.out);
+    g.lse = a.lse;
+    static unsigned long long done = 0;
+    cudaError_t e = smem_limit_once(attn_gather_tc_kernel, (int)kSmemBytes, done);
+    if (e != cudaSuccess) return e;
+    const int grid = a.rows < num_sms ? a.rows : num_sms;
+    attn_gather_tc_kernel<<<grid, kThreads, kSmemBytes, s>>>(tq, g);
+    return cudaGetLastError();
+}
+
+}  // namespace hsa

@@ -426,6 +426,8 @@ hsa_status_t hsa_attn_prefill(const void *q, hsa_dtype_t dt, int B, int T, int H
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (dt == HSA_BF16 && hsa::prefill_tc_supported(a))
         return launched(hsa::launch_attn_prefill_tc(a, di.num_sms, s), "attn_prefill (tcgen05)");
+    if (dt == HSA_BF16 && hsa::gather_tc_supported(a))
+        return launched(hsa::launch_attn_gather_tc(a, di.num_sms, s), "attn_prefill (tcgen05 gather)");
     cudaError_t e = dt == HSA_BF16 ? hsa::launch_attn_bf16(a, s) : hsa::launch_attn_f32(a, s);
     return launched(e, "attn_prefill");
 }

@@ -184,5 +184,8 @@ cudaError_t launch_attn_decode_cluster(const AttnArgs &a, cudaStream_t s);
 // bf16 dense (HCA) prefill with d = 128 and T*H a multiple of 128: tcgen05 + TMA kernel.
 bool prefill_tc_supported(const AttnArgs &a);
 cudaError_t launch_attn_prefill_tc(const AttnArgs &a, int num_sms, cudaStream_t s);
+// bf16 CSA prefill with H = 64 and d = 128: per-token gathers, tcgen05 M = 64 MMAs.
+bool gather_tc_supported(const AttnArgs &a);
+cudaError_t launch_attn_gather_tc(const AttnArgs &a, int num_sms, cudaStream_t s);
 
 }  // namespace hsa
