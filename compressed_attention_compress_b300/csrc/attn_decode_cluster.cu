@@ -117,6 +117,10 @@ __global__ void __launch_bounds__(NW * 32) attn_decode_cluster_kernel(AttnArgs a
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int b = row;  // decode: one query per sequence
     const bool dense = a.idx == nullptr;
+    // launched with programmatic stream serialization: wait until the preceding grid
+    // (normally the indexer) has completed and its writes are visible, before any
+    // input is read (a no-op when there is no such dependency)
+    asm volatile("griddepcontrol.wait;\n" ::: "memory");
 
     // ---- first round trip: Q, position, count and (CSA) this slice's indices
     {
@@ -394,13 +398,17 @@ cudaError_t launch_cluster_t(const AttnArgs &a, cudaStream_t s) {
     cfg.blockDim = dim3(NW * 32);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = S;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    // the launch may overlap the tail of the previous kernel in the stream; the
+    // kernel's first instruction waits for that kernel's completion
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, attn_decode_cluster_kernel<D, NW, 16>, a);
 }
 

@@ -117,6 +117,10 @@ __device__ __forceinline__ void find_threshold(const unsigned *hist, int nb, int
 
 template <int LPE>
 __global__ void __launch_bounds__(kThreads) index_fused_kernel(IndexArgs a, FusedIndexPlan p, void *ws) {
+    // a kernel launched after this one with programmatic stream serialization (the
+    // decode attention) may be scheduled now; it waits for this grid's completion
+    // before it reads anything
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
     extern __shared__ __align__(16) unsigned char smem[];
     uint32_t *s_keys = reinterpret_cast<uint32_t *>(smem);          // [chunk], kept over all phases
     unsigned *s_h = reinterpret_cast<unsigned *>(smem + (size_t)p.chunk * 4);  // [max(kNB1, nb2)]
