@@ -44,10 +44,10 @@ WL = WORKLOADS["pro_csa_decode"]
 # ncu capture summarised in profiles/index_fused_kernel_pro_csa_1M_B4.md; reported only
 # while the kernel's sources are the ones that capture ran.
 INDEX_TRAFFIC = {
-    "bytes": 67210240 + 216320,
+    "bytes": 67210240 + 207104,
     "sources": {
         "compressed_attention_compress_b300/csrc/index_fused.cu":
-            "28f7a328141842f9f3275299914034562505ac39713cf05675294f3c4d73ceb5",
+            "45fab5ff0d11b0d0993b7e1caaa948ba9600dabb8db8f34c338c31e2c604dade",
         "compressed_attention_compress_b300/csrc/common.cuh":
             "35428b34db55a12ea4c19016f4b5a1d3dbe35eca7162b0449b366e789980467b",
         "compressed_attention_compress_b300/csrc/block_scan.cuh":
