@@ -3,23 +3,24 @@
 // QbitAI article "DeepSeek V4报告太详尽了！", section 混合注意力机制, CSA step 2 (score every
 // visible compressed entry against the query, keep the top-k).  Same result as
 // the two-kernel path in index_topk.cu, in one launch whose CTAs of a row meet
-// at two row barriers (the launch is cooperative, so all CTAs are resident and
-// every barrier completes; each wait is still bounded and raises the device
-// flag if it ever gives up):
+// once at a row barrier (the launch is cooperative, so all CTAs are resident and
+// the barrier completes; each wait is still bounded and raises the device flag
+// if it ever gives up):
 //   phase 1  dp4a scores of this CTA's chunk, kept in shared memory as biased
 //            keys u = s + DI*16256; a 2048-bin histogram of u >> shift1 is
 //            merged into the row's global histogram.               -- barrier
 //   phase 2  every CTA reads the row histogram and finds the bin b1 holding
-//            the k-th largest key; it publishes its count of keys above b1
-//            and appends its keys inside b1 to the row's in-bin list.  -- barrier
-//   phase 3  every CTA resolves the exact threshold key T and the number of
-//            ties at T to take (by ascending index) from the small in-bin list,
-//            then writes its own chunk's winners, in index order, at the
-//            offset given by the earlier chunks.  The last CTA to finish
-//            returns the row's histogram and counters to zero.
-// If the in-bin list overflows its capacity (heavily tied scores) the keys are
-// spilled to the workspace and the first CTA of the row does an exact
-// row-wide pass instead.
+//            the k-th largest key; it writes its keys in bins >= b1 (key,
+//            index), in index order, to its chunk's region of the row's
+//            candidate list, and their count.  An atomic counter finds the last
+//            CTA of the row to get here; the others leave.
+//   phase 3  the last CTA reads the candidate list chunk after chunk (so in
+//            index order), resolves the exact threshold key T inside b1 with a
+//            level-2 histogram, takes the keys above T and the first ties at T,
+//            writes the row's output and returns the row's histogram and
+//            counter to zero.
+// A chunk's region holds its whole chunk, so heavily tied scores (many keys in
+// b1) only make phase 3 longer.
 #include "block_scan.cuh"
 #include "common.cuh"
 #include "internal.h"
@@ -32,8 +33,6 @@ constexpr int kThreads = 256;
 constexpr int kNB1 = 2048;
 constexpr unsigned long long kSpinLimit = 1ull << 24;
 constexpr int kStages = 3;
-constexpr int kSlot = 7;     // in-bin (key, index) pairs carried by a chunk record
-constexpr int kBrute = 512;  // in-bin lists up to this size are ranked by brute force
 constexpr int kStageBytes = 16384;
 
 __device__ __forceinline__ unsigned ld_acquire(const unsigned *p) {
@@ -74,21 +73,17 @@ __device__ __forceinline__ int dot16(const int4 &x, const int4 &y) {
 
 struct Ws {
     unsigned *hist1;  // [rows][kNB1]
-    unsigned *bar;    // [rows][4]: barrier, in-bin count, exit count, pad
-    uint32_t *in_u;   // [rows][cap_in]
-    int32_t *in_j;    // [rows][cap_in]
-    uint32_t *keys;   // [rows][C*chunk] (heavy ties only)
-    int *rec;         // [rows][C][16] chunk records
+    unsigned *bar;    // [rows][4]: row counter, pad
+    int *rec;         // [rows][C] candidates per chunk
+    uint2 *cand;      // [rows][C * chunk] (key, index) in bins >= b1, chunk c at c * chunk
 };
 __device__ __forceinline__ Ws carve(void *ws, const FusedIndexPlan &p, int r) {
     char *b = static_cast<char *>(ws);
     Ws w;
     w.hist1 = reinterpret_cast<unsigned *>(b + p.off_hist1) + (size_t)r * kNB1;
     w.bar = reinterpret_cast<unsigned *>(b + p.off_bar) + (size_t)r * 4;
-    w.in_u = reinterpret_cast<uint32_t *>(b + p.off_in_u) + (size_t)r * p.cap_in;
-    w.in_j = reinterpret_cast<int32_t *>(b + p.off_in_j) + (size_t)r * p.cap_in;
-    w.keys = reinterpret_cast<uint32_t *>(b + p.off_keys) + (size_t)r * p.ctas_per_row * p.chunk;
-    w.rec = reinterpret_cast<int *>(b + p.off_rec) + (size_t)r * p.ctas_per_row * 16;
+    w.rec = reinterpret_cast<int *>(b + p.off_rec) + (size_t)r * p.ctas_per_row;
+    w.cand = reinterpret_cast<uint2 *>(b + p.off_cand) + (size_t)r * p.ctas_per_row * p.chunk;
     return w;
 }
 
@@ -237,21 +232,13 @@ __global__ void __launch_bounds__(kThreads) index_fused_kernel(IndexArgs a, Fuse
     if (!row_barrier(&w.bar[0], (unsigned)nch, &s_misc[7])) return;
 
     // ---------------------------------------------------------------- phase 2
-    // One read of the row histogram gives b1; this chunk publishes a fixed-size
-    // record {keys above b1, keys in b1, up to kSlot (key, index) pairs in b1}
-    // with plain stores; in-bin keys beyond kSlot go to the row overflow list.
-    __shared__ int s_cnt_above, s_cnt_in, s_list_n, s_above_before, s_sel_before;
-    __shared__ uint32_t s_slot_u[kSlot];
-    __shared__ int32_t s_slot_j[kSlot];
-    constexpr int PB = kNB1 / kThreads;  // bins per thread, descending
-    if (threadIdx.x == 0) {
-        s_cnt_above = 0;
-        s_cnt_in = 0;
-        s_list_n = 0;
-        s_above_before = 0;
-        s_sel_before = 0;
-    }
+    // One read of the row histogram gives b1; this chunk appends its keys in bins
+    // >= b1, as (key, index) in index order, to its region of the row's candidate
+    // list and records how many.  The last CTA of the row to get here does phase 3;
+    // the others leave.
     {
+        constexpr int PB = kNB1 / kThreads;  // bins per thread, descending
+        if (threadIdx.x == 0) s_misc[0] = s_misc[1] = s_misc[2] = 0;  // set below; defined even if never found
         const int top = kNB1 - 1 - threadIdx.x * PB;
         int hv[PB];
         int local = 0;
@@ -278,214 +265,202 @@ __global__ void __launch_bounds__(kThreads) index_fused_kernel(IndexArgs a, Fuse
         __syncthreads();
     }
     const int b1 = s_misc[0], count_above = s_misc[1], n_in = s_misc[2];
-    const bool spill = n_in > p.cap_in;  // heavily tied scores: exact pass over spilled keys
-    const int per = (p.chunk + kThreads - 1) / kThreads;
-    const int my0 = threadIdx.x * per;
     {
-        int above = 0;
+        const int per = (p.chunk + kThreads - 1) / kThreads;
+        const int my0 = threadIdx.x * per;
+        int nc = 0;
         for (int q = 0; q < per; ++q) {
+            const int e = my0 + q;
+            if (e < n) nc += (int)(s_keys[e] >> p.shift1) >= b1;
+        }
+        int tot;
+        int o = block_exclusive_sum(nc, s_scan, tot);
+        uint2 *cand = w.cand + c0;
+        for (int q = 0; q < per && nc; ++q) {
             const int e = my0 + q;
             if (e < n) {
                 const uint32_t u = s_keys[e];
-                const int bin = (int)(u >> p.shift1);
-                above += bin > b1;
-                if (bin == b1) {
-                    const int k = atomicAdd(&s_cnt_in, 1);
-                    if (k < kSlot) {
-                        s_slot_u[k] = u;
-                        s_slot_j[k] = (int32_t)(c0 + e);
-                    } else if (!spill) {
-                        const unsigned o = atomicAdd(&w.bar[1], 1u);
-                        if (o < (unsigned)p.cap_in) {
-                            w.in_u[o] = u;
-                            w.in_j[o] = (int32_t)(c0 + e);
-                        }
-                    }
+                if ((int)(u >> p.shift1) >= b1) {
+                    cand[o++] = make_uint2(u, (uint32_t)(c0 + e));
+                    --nc;
                 }
             }
         }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) above += __shfl_xor_sync(0xffffffffu, above, o);
-        if ((threadIdx.x & 31) == 0 && above) atomicAdd(&s_cnt_above, above);
+        if (threadIdx.x == 0) w.rec[c] = tot;
     }
-    __syncthreads();
-    if (threadIdx.x < 16) {
-        // record layout: {above, n_in, (u0, j0), ..., (u6, j6)}; unused pairs carry j = -1
-        int v;
-        if (threadIdx.x == 0) v = s_cnt_above;
-        else if (threadIdx.x == 1) v = s_cnt_in;
-        else {
-            const int k = (threadIdx.x - 2) >> 1;
-            const bool has = k < s_cnt_in && k < kSlot;
-            v = (threadIdx.x & 1) == 0 ? (has ? (int)s_slot_u[k] : 0) : (has ? s_slot_j[k] : -1);
-        }
-        w.rec[(size_t)c * 16 + threadIdx.x] = v;
-    }
-    if (spill)
-        for (int e = threadIdx.x; e < n; e += kThreads) w.keys[c0 + e] = s_keys[e];
-    if (!row_barrier(&w.bar[0], 2u * (unsigned)nch, &s_misc[7])) return;
-
-    // ---------------------------------------------------------------- phase 3
-    const int need = kE - count_above;  // >= 1
-    if (!spill) {
-        // One read of every chunk's record (and of the overflow count) builds the
-        // in-bin list in shared memory (the copy stages are free by now).
-        uint2 *s_l = reinterpret_cast<uint2 *>(smem + p.off_stage_smem);  // [cap_in] (key, index)
-        const int4 *rec4 = reinterpret_cast<const int4 *>(w.rec);
-        int above_before = 0;
-        for (int r = threadIdx.x; r < nch * 4; r += kThreads) {
-            const int4 v = __ldcg(&rec4[r]);
-            const int cc = r >> 2, qq = r & 3;
-            if (qq == 0 && cc < c) above_before += v.x;
-            if (qq != 0 && v.y >= 0) {
-                const int k = atomicAdd(&s_list_n, 1);
-                if (k < p.cap_in) s_l[k] = make_uint2((uint32_t)v.x, (uint32_t)v.y);
-            }
-            if (v.w >= 0) {
-                const int k = atomicAdd(&s_list_n, 1);
-                if (k < p.cap_in) s_l[k] = make_uint2((uint32_t)v.z, (uint32_t)v.w);
-            }
-        }
-        const int n_ovf = (int)min(__ldcg(&w.bar[1]), (unsigned)p.cap_in);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) above_before += __shfl_xor_sync(0xffffffffu, above_before, o);
-        if ((threadIdx.x & 31) == 0 && above_before) atomicAdd(&s_above_before, above_before);
-        for (int i = threadIdx.x; i < n_ovf; i += kThreads) {
-            const int k = atomicAdd(&s_list_n, 1);
-            if (k < p.cap_in) s_l[k] = make_uint2(__ldcg(&w.in_u[i]), (uint32_t)__ldcg(&w.in_j[i]));
-        }
-        __syncthreads();
-        const int nl = min(s_list_n, p.cap_in);  // == n_in
-        // Decide every in-bin key; count the selected ones that precede this chunk
-        // and mark those inside it (bit 31 of its shared-memory key; keys < 2^23).
-        int sel_before = 0;
-        auto settle = [&](uint32_t j, bool take) {
-            if (!take) return;
-            if ((int64_t)j < c0) ++sel_before;
-            else if ((int64_t)j < c0 + n) s_keys[j - c0] |= 0x80000000u;
-        };
-        if (nl <= kBrute) {
-            // rank = in-bin keys that beat key i under (key desc, index asc)
-            for (int i = threadIdx.x; i < nl; i += kThreads) {
-                const uint2 me = s_l[i];
-                int rank = 0;
-#pragma unroll 8
-                for (int k = 0; k < nl; ++k) {
-                    const uint2 o = s_l[k];
-                    rank += (o.x > me.x) | ((o.x == me.x) & (o.y < me.y));
-                }
-                settle(me.y, rank < need);
-            }
-        } else {
-            // level-2 histogram over the low bits of the in-bin keys
-            unsigned *s_h2 = s_h;
-            const uint32_t mask2 = (uint32_t)p.nb2 - 1u;
-            for (int i = threadIdx.x; i < p.nb2; i += kThreads) s_h2[i] = 0;
-            __syncthreads();
-            for (int i = threadIdx.x; i < nl; i += kThreads) atomicAdd(&s_h2[s_l[i].x & mask2], 1u);
-            __syncthreads();
-            find_threshold(s_h2, p.nb2, need, s_scan, &s_misc[4]);
-            const uint32_t T = ((uint32_t)b1 << p.shift1) | (uint32_t)s_misc[4];
-            const int n_eq_need = need - s_misc[5];
-            for (int i = threadIdx.x; i < nl; i += kThreads) {
-                const uint2 me = s_l[i];
-                bool take = me.x > T;
-                if (me.x == T) {
-                    int er = 0;
-                    for (int k = 0; k < nl; ++k) er += (s_l[k].x == T) & (s_l[k].y < me.y);
-                    take = er < n_eq_need;
-                }
-                settle(me.y, take);
-            }
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) sel_before += __shfl_xor_sync(0xffffffffu, sel_before, o);
-        if ((threadIdx.x & 31) == 0 && sel_before) atomicAdd(&s_sel_before, sel_before);
-        __syncthreads();
-        const int base = s_above_before + s_sel_before;
-        // this chunk, in index order
-        auto taken = [&](uint32_t u) {
-            return (int)((u & 0x7fffffffu) >> p.shift1) > b1 || (u & 0x80000000u);
-        };
-        int nsel = 0;
-        for (int q = 0; q < per; ++q) {
-            const int e = my0 + q;
-            if (e < n) nsel += taken(s_keys[e]);
-        }
-        int tot;
-        int o = base + block_exclusive_sum(nsel, s_scan, tot);
-        for (int q = 0; q < per; ++q) {
-            const int e = my0 + q;
-            if (e < n && taken(s_keys[e])) idx_out[o++] = (int32_t)(c0 + e);
-        }
-    } else if (c == 0) {
-        // exact row-wide pass over the spilled keys (heavily tied scores)
-        unsigned *s_h2 = s_h;
-        const uint32_t mask2 = (uint32_t)p.nb2 - 1u;
-        for (int i = threadIdx.x; i < p.nb2; i += kThreads) s_h2[i] = 0;
-        __syncthreads();
-        for (int64_t e = threadIdx.x; e < E; e += kThreads) {
-            const uint32_t u = __ldcg(&w.keys[e]);
-            if ((int)(u >> p.shift1) == b1) atomicAdd(&s_h2[u & mask2], 1u);
-        }
-        __syncthreads();
-        find_threshold(s_h2, p.nb2, need, s_scan, &s_misc[4]);
-        const uint32_t T = ((uint32_t)b1 << p.shift1) | (uint32_t)s_misc[4];
-        const int n_eq_need = need - s_misc[5];
-        constexpr int PER = 16;
-        int eq_base = 0, pos_base = 0;
-        for (int64_t t0 = 0; t0 < E; t0 += (int64_t)kThreads * PER) {
-            const int64_t m0 = t0 + (int64_t)threadIdx.x * PER;
-            uint32_t uu[PER];
-            int eq = 0;
-#pragma unroll
-            for (int q = 0; q < PER; ++q) {
-                const int64_t e = m0 + q;
-                uu[q] = e < E ? __ldcg(&w.keys[e]) : 0u;
-                eq += (e < E && uu[q] == T);
-            }
-            int tot_eq, tot_sel;
-            int er = eq_base + block_exclusive_sum(eq, s_scan, tot_eq);
-            int nsel = 0;
-            {
-                int er2 = er;
-#pragma unroll
-                for (int q = 0; q < PER; ++q) {
-                    if (m0 + q >= E) break;
-                    if (uu[q] > T) ++nsel;
-                    else if (uu[q] == T) { nsel += er2 < n_eq_need; ++er2; }
-                }
-            }
-            int o = pos_base + block_exclusive_sum(nsel, s_scan, tot_sel);
-#pragma unroll
-            for (int q = 0; q < PER; ++q) {
-                const int64_t e = m0 + q;
-                if (e >= E) break;
-                bool take = uu[q] > T;
-                if (uu[q] == T) { take = er < n_eq_need; ++er; }
-                if (take) idx_out[o++] = (int32_t)e;
-            }
-            eq_base += tot_eq;
-            pos_base += tot_sel;
-        }
-    }
-
-    // ---------------------------------------------------------------- exit
+    // every thread's candidates are ordered before thread 0's fence by the block
+    // barrier; the fence and the counter publish them to the row's last CTA
     __syncthreads();
     if (threadIdx.x == 0) {
         __threadfence();
-        s_misc[6] = atomicAdd(&w.bar[2], 1u) == (unsigned)(nch - 1);
+        s_misc[6] = atomicAdd(&w.bar[0], 1u) == 2u * (unsigned)nch - 1u;
     }
     __syncthreads();
-    if (s_misc[6]) {
-        __threadfence();
-        for (int i = threadIdx.x; i < kNB1; i += kThreads) w.hist1[i] = 0;
+    if (!s_misc[6]) return;
+    __threadfence();
+
+    // ---------------------------------------------------------------- phase 3
+    // (last CTA of the row) The chunks' regions, one after another, list every key
+    // in bins >= b1 in index order.  The first `spec` slots of every region are
+    // loaded together with the regions' counts (slots past a count are never
+    // used), so a typical row needs one round trip to L2; longer regions are read
+    // by one flat pass over all threads.  The list is staged in shared memory in
+    // index order while a level-2 histogram of the low bits of the keys in b1 is
+    // built; it gives the threshold key T and how many keys equal to T to take (the
+    // first ones in index order).  One ordered pass writes the winners.
+    int *s_off = reinterpret_cast<int *>(smem + p.off_stage_smem);  // [nch + 1] list offsets
+    int *s_roff = s_off + (nch + 1);                                 // [nch + 1] offsets past the first spec slots
+    const int l_off = (2 * (nch + 1) * 4 + 15) & ~15;
+    uint2 *s_l = reinterpret_cast<uint2 *>(smem + p.off_stage_smem + l_off);
+    const int l_cap = (kStages * kStageBytes - l_off) / 8;
+    unsigned *s_h2 = s_h;
+    const uint32_t mask2 = (uint32_t)p.nb2 - 1u;
+    for (int i = threadIdx.x; i < p.nb2; i += kThreads) s_h2[i] = 0;
+    if (threadIdx.x == 0) s_misc[4] = s_misc[5] = 0;  // set by find_threshold; defined even if never found
+    constexpr int kSpecPer = 16;  // speculative slot loads per thread
+    int lg_spec = 5;
+    while (lg_spec > 0 && (nch << lg_spec) > kThreads * kSpecPer) --lg_spec;
+    const int spec = (nch << lg_spec) <= kThreads * kSpecPer ? 1 << lg_spec : 0;
+    uint2 sv[kSpecPer];
+#pragma unroll
+    for (int q = 0; q < kSpecPer; ++q) {
+        const int sp = q * kThreads + threadIdx.x;
+        const int cc = spec ? sp >> lg_spec : nch;
+        sv[q] = cc < nch ? __ldcg(w.cand + (int64_t)cc * p.chunk + (sp & (spec - 1))) : make_uint2(0u, 0u);
+    }
+    const int cpt = (nch + kThreads - 1) / kThreads;  // chunks per thread for the scans
+    const int i0 = threadIdx.x * cpt;
+    {
+        int loc = 0, rest = 0;
+        for (int q = 0; q < cpt; ++q)
+            if (i0 + q < nch) {
+                const int v = __ldcg(&w.rec[i0 + q]);
+                s_off[i0 + q] = v;
+                loc += v;
+                rest += v > spec ? v - spec : 0;
+            }
+        int tot, rtot;
+        int o = block_exclusive_sum(loc, s_scan, tot);
+        int ro = block_exclusive_sum(rest, s_scan, rtot);
+        for (int q = 0; q < cpt; ++q)
+            if (i0 + q < nch) {
+                const int v = s_off[i0 + q];
+                s_off[i0 + q] = o;
+                s_roff[i0 + q] = ro;
+                o += v;
+                ro += v > spec ? v - spec : 0;
+            }
         if (threadIdx.x == 0) {
-            w.bar[0] = 0;
-            w.bar[1] = 0;
-            w.bar[2] = 0;
+            s_off[nch] = tot;
+            s_roff[nch] = rtot;
+        }
+        __syncthreads();
+    }
+    const int total = s_off[nch], n_rest = s_roff[nch];
+    if (total != count_above + n_in && threadIdx.x == 0) raise_flag(FLAG_INDEX_RANGE | 0x400u);
+    const bool staged = total <= l_cap;
+    const int need = kE - count_above;  // >= 1
+    auto take_in = [&](const uint2 &v, int L) {
+        if (staged) s_l[L] = v;
+        if ((int)(v.x >> p.shift1) == b1) atomicAdd(&s_h2[v.x & mask2], 1u);
+    };
+#pragma unroll
+    for (int q = 0; q < kSpecPer; ++q) {
+        const int sp = q * kThreads + threadIdx.x;
+        const int cc = spec ? sp >> lg_spec : nch;
+        if (cc < nch) {
+            const int i = sp & (spec - 1);
+            if (i < s_off[cc + 1] - s_off[cc]) take_in(sv[q], s_off[cc] + i);
         }
     }
+    // last c with off[c] <= L (off ascending over [0, nch])
+    auto find_chunk = [&](const int *off, int L) {
+        int lo = 0, hi = nch - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (off[mid] <= L) lo = mid;
+            else hi = mid - 1;
+        }
+        return lo;
+    };
+    constexpr int PER = 8;
+    for (int t0 = 0; t0 < n_rest; t0 += kThreads * PER) {
+        uint2 v[PER];
+        int lpos[PER];
+#pragma unroll
+        for (int q = 0; q < PER; ++q) {
+            const int R = t0 + q * kThreads + threadIdx.x;
+            lpos[q] = -1;
+            if (R < n_rest) {
+                const int cc = find_chunk(s_roff, R);
+                const int i = spec + (R - s_roff[cc]);
+                lpos[q] = s_off[cc] + i;
+                v[q] = __ldcg(w.cand + (int64_t)cc * p.chunk + i);
+            }
+        }
+#pragma unroll
+        for (int q = 0; q < PER; ++q)
+            if (lpos[q] >= 0) take_in(v[q], lpos[q]);
+    }
+    __syncthreads();
+    find_threshold(s_h2, p.nb2, need, s_scan, &s_misc[4]);
+    const uint32_t T = ((uint32_t)b1 << p.shift1) | (uint32_t)s_misc[4];
+    const int n_eq_need = need - s_misc[5];
+    const bool all_eq = n_eq_need == (int)s_h2[s_misc[4]];  // every key equal to T is taken
+    int eq_base = 0, pos_base = 0;
+    for (int t0 = 0; t0 < total; t0 += kThreads * PER) {
+        const int m0 = t0 + threadIdx.x * PER;
+        uint2 v[PER];
+#pragma unroll
+        for (int q = 0; q < PER; ++q) {
+            const int L = m0 + q;
+            if (L >= total) v[q] = make_uint2(0u, 0u);
+            else if (staged) v[q] = s_l[L];
+            else {
+                const int cc = find_chunk(s_off, L);
+                v[q] = __ldcg(w.cand + (int64_t)cc * p.chunk + (L - s_off[cc]));
+            }
+        }
+        bool take[PER];
+        int nsel = 0;
+        if (all_eq) {
+#pragma unroll
+            for (int q = 0; q < PER; ++q) {
+                take[q] = m0 + q < total && v[q].x >= T;
+                nsel += take[q];
+            }
+        } else {
+            int eq = 0;
+#pragma unroll
+            for (int q = 0; q < PER; ++q) eq += m0 + q < total && v[q].x == T;
+            int tot_eq;
+            int er = eq_base + block_exclusive_sum(eq, s_scan, tot_eq);
+#pragma unroll
+            for (int q = 0; q < PER; ++q) {
+                take[q] = m0 + q < total && v[q].x > T;
+                if (m0 + q < total && v[q].x == T) {
+                    take[q] = er < n_eq_need;
+                    ++er;
+                }
+                nsel += take[q];
+            }
+            eq_base += tot_eq;
+        }
+        int tot_sel;
+        int o = pos_base + block_exclusive_sum(nsel, s_scan, tot_sel);
+#pragma unroll
+        for (int q = 0; q < PER; ++q)
+            if (take[q]) {
+                if (o < kE) idx_out[o] = (int32_t)v[q].y;
+                else raise_flag(FLAG_INDEX_RANGE | 0x400u);
+                ++o;
+            }
+        pos_base += tot_sel;
+    }
+
+    // the row's histogram and counter return to zero for the next launch
+    for (int i = threadIdx.x; i < kNB1; i += kThreads) w.hist1[i] = 0;
+    if (threadIdx.x == 0) w.bar[0] = 0;
 }
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -542,7 +517,6 @@ FusedIndexPlan plan_index_fused(int rows, int DI, int64_t E_cap, int num_sms) {
     p.key_bits = key_bits_for(DI);
     p.shift1 = p.key_bits - 11;
     p.nb2 = 1 << p.shift1;
-    p.cap_in = 4096;
     // Chunks are multiples of 64 entries; pick the smallest chunk whose launch
     // (ceil(E/chunk) CTAs per row) is resident all at once, so every SM streams
     // an equal share.
@@ -569,13 +543,9 @@ FusedIndexPlan plan_index_fused(int rows, int DI, int64_t E_cap, int num_sms) {
     p.off_bar = off;
     off = align256(off + sizeof(unsigned) * 4 * (size_t)rows);
     p.off_rec = off;
-    off = align256(off + sizeof(int) * 16 * (size_t)p.ctas_per_row * rows);
-    p.off_in_u = off;
-    off = align256(off + sizeof(uint32_t) * (size_t)p.cap_in * rows);
-    p.off_in_j = off;
-    off = align256(off + sizeof(int32_t) * (size_t)p.cap_in * rows);
-    p.off_keys = off;
-    off = align256(off + sizeof(uint32_t) * (size_t)p.ctas_per_row * p.chunk * rows);
+    off = align256(off + sizeof(int) * (size_t)p.ctas_per_row * rows);
+    p.off_cand = off;
+    off = align256(off + sizeof(uint2) * (size_t)p.ctas_per_row * p.chunk * rows);
     p.total = off;
     return p;
 }

@@ -74,10 +74,10 @@ cudaError_t launch_index_topk(const IndexArgs &a, const IndexPlan &p, void *ws, 
 // Decode-shaped indexer: one cooperative launch (index_fused.cu).
 struct FusedIndexPlan {
     bool ok;           // false: the rows do not fit one resident launch
-    int rows, ctas_per_row, chunk, key_bits, shift1, nb2, cap_in;
+    int rows, ctas_per_row, chunk, key_bits, shift1, nb2;
     int off_stage_smem;  // byte offset of the copy stages in dynamic shared memory
     size_t smem;
-    size_t off_hist1, off_bar, off_rec, off_in_u, off_in_j, off_keys, total;
+    size_t off_hist1, off_bar, off_rec, off_cand, total;
 };
 FusedIndexPlan plan_index_fused(int rows, int DI, int64_t E_cap, int num_sms);
 cudaError_t launch_index_fused(const IndexArgs &a, const FusedIndexPlan &p, void *ws, cudaStream_t s);

@@ -113,6 +113,19 @@ def test_index_topk_heavy_ties_fast_and_fallback(lib):
     _index_case(lib, B=1, T=1, E_cap=20000, DI=64, m=4, topk=777, pos0=[4 * 20000 - 1], k_idx=z, seed=4)
 
 
+def test_index_topk_concentrated_run(lib):
+    # every top key sits in one contiguous run, so a few chunks hold all the
+    # candidates; row 1 also splits a tie at the threshold by index
+    E_cap, DI, k, seed = 100000, 64, 1024, 11
+    q = _randint8((2, 1, DI), 100 + seed, -127, 127)
+    kI = _randint8((2, E_cap, DI), 12, -3, 3)
+    kI[0, 40000:41500] = q[0, 0]
+    kI[1, 70000:70700] = q[1, 0]
+    kI[1, 70700:71200] = torch.div(q[1, 0], 2, rounding_mode="trunc")
+    _index_case(lib, B=2, T=1, E_cap=E_cap, DI=DI, m=4, topk=k, pos0=[4 * E_cap - 1, 4 * E_cap - 1], k_idx=kI,
+                seed=seed)
+
+
 def test_index_topk_extreme_values(lib):
     # -128 everywhere: largest possible scores, all tied
     kI = torch.full((1, 5000, 64), -128, dtype=torch.int8)
