@@ -1,0 +1,399 @@
+// Decode attention (one query token per sequence) over the selected entries plus
+// the window of a CSA layer, bf16, d = 128, H a multiple of 64, on the
+// 5th-generation tensor cores.
+//
+// QbitAI article "DeepSeek V4报告太详尽了！", section 混合注意力机制: CSA step 3 (MQA over
+// the top-k compressed entries the indexer selected) and the sliding-window
+// paragraph (the most recent raw tokens join the same softmax).
+//
+// A sequence's item slots (topk selected entries, then the window tokens) are cut
+// into tiles of 128 items; tile j of a (sequence, 64-head group) is CTA j of a
+// cluster of n_tiles CTAs.  Each CTA
+//   - gathers its tile's K and V rows with cp.async into 128-byte-swizzled shared
+//     memory (zero-filled for invalid slots, a 128-bit validity mask beside it);
+//   - computes S = Q K^T (M = 64 heads, N = 128 items, K = d) into TMEM, one
+//     thread issuing tcgen05.mma (row h of an M = 64 accumulator sits in TMEM lane
+//     (h / 16) * 32 + h % 16, so lanes 0-15 of warp w hold heads 16w..16w+15);
+//   - takes the masked softmax of its tile, one head per thread, writes P (bf16)
+//     to shared memory and accumulates O = P V into TMEM;
+//   - keeps its unnormalised partial (O, maximum, sum) in shared memory.
+// After a cluster barrier CTA r combines heads [r * hpc, (r + 1) * hpc) of all the
+// partials through distributed shared memory with the log-sum-exp rule and writes
+// the output and the log-sum-exp.  Q, the TMEM allocation and tiles that hold only
+// window tokens need nothing from the indexer, so they run before the kernel waits
+// for the preceding grid (the launch uses programmatic stream serialization).
+// Every wait is bounded; a wait that gives up raises the device flag, and the CTA
+// still reaches both cluster barriers and frees its TMEM.
+#include <math.h>
+
+#include "internal.h"
+#include "tc_common.cuh"
+
+namespace hsa {
+
+namespace {
+
+constexpr int kH = 64;                  // heads per CTA = MMA M
+constexpr int kD = 128;                 // head dim
+constexpr int kN = 128;                 // items per tile = MMA N of S
+constexpr int kThreads = 128;
+constexpr int kMaxTiles = 16;           // cluster size limit
+constexpr int kQBlk = kH * 128;         // 8 KiB: one 64-column block of Q or P
+constexpr int kQBytes = 2 * kQBlk;      // 16 KiB
+constexpr int kTBlk = kN * 128;         // 16 KiB: one 64-column block of a K or V tile
+constexpr int kTile = 2 * kTBlk;        // 32 KiB
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr unsigned long long kWaitLimit = 1ull << 22;
+// dynamic shared memory: 1 KiB for alignment | Q | K tile | V tile | P; the fp32
+// partial O [64][128] (32 KiB) reuses the K tile once both MMAs are done
+constexpr size_t kSmemBytes = 1024 + (size_t)kQBytes + 2 * (size_t)kTile + (size_t)kQBytes;
+
+struct DecodeTcArgs {
+    int B, H, topk, window, m, n_tiles, shared_kv;
+    int64_t E_cap, N_cap, c_sb, c_se, r_sb, r_st;
+    const int64_t *ctx;          // [B]: the query sits at p = ctx - 1
+    const int32_t *idx, *cnt;    // [B, topk], [B] or null
+    const __nv_bfloat16 *q, *kc, *vc, *k_raw, *v_raw;
+    float scale_log2;
+    __nv_bfloat16 *out;          // [B, H, d]
+    float *lse;                  // [B, H] or null
+};
+
+// chunk c (16 bytes) of row r of a 128-byte-swizzled K-major tile made of 64-column blocks
+__device__ __forceinline__ uint32_t sw_off(int r, int c, int blk_bytes) {
+    return (uint32_t)((c >> 3) * blk_bytes + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+}
+// float4 chunk c4 of row h of the fp32 partial O, rotated so that the 16 heads a
+// warp stores at once spread over the banks
+__device__ __forceinline__ int o_off(int h, int c4) { return h * kD + ((c4 ^ (h & 31)) << 2); }
+
+__device__ __forceinline__ bool wait_phase0(uint64_t *bar) {
+    for (unsigned long long i = 0; i < kWaitLimit; ++i)
+        if (mbar_try_wait(bar, 0u)) return true;
+    return false;
+}
+
+__global__ void __launch_bounds__(kThreads, 1) attn_decode_tc_kernel(DecodeTcArgs a) {
+    extern __shared__ __align__(16) unsigned char smem_raw[];  // rounded up to 1024 at run time
+    unsigned char *smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+    unsigned char *sQ = smem;
+    unsigned char *sK = sQ + kQBytes;
+    unsigned char *sV = sK + kTile;
+    unsigned char *sP = sV + kTile;
+    float *sO = reinterpret_cast<float *>(sK);
+    __shared__ float sM[kH], sL[kH];
+    __shared__ uint32_t s_mask[kThreads / 32];
+    __shared__ __align__(8) uint64_t bar_s, bar_o;
+    __shared__ uint32_t s_tmem;
+
+    const int j = blockIdx.x;  // tile == rank in the cluster
+    const int b = blockIdx.y, hg = blockIdx.z;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+    if (tid == 0) {
+        mbar_init(&bar_s, 1);
+        mbar_init(&bar_o, 1);
+        fence_mbar_init();
+    }
+    if (warp == 0) tc::tmem_alloc(&s_tmem, 256);  // S: columns [0, 128), O: [128, 256)
+    // Q of this head group into 128-byte-swizzled K-major rows (cp.async group 0)
+    {
+        const __nv_bfloat16 *q = a.q + ((int64_t)b * a.H + (int64_t)hg * kH) * kD;
+        for (int i = tid; i < kH * 16; i += kThreads) {
+            const int h = i >> 4, c = i & 15;
+            cp_async_16(smem_u32(sQ + sw_off(h, c, kQBlk)), q + (int64_t)h * kD + c * 8, 16);
+        }
+        cp_async_commit();
+    }
+    const int64_t p = a.ctx[b] - 1;
+    int64_t E = num_entries(p, a.m);
+    if (E > a.E_cap) E = a.E_cap;
+    const int slot0 = j * kN;
+    // the indexer's output (idx, cnt) is read only by tiles holding selected-entry slots
+    if (slot0 < a.topk) asm volatile("griddepcontrol.wait;\n" ::: "memory");
+
+    // ---- the item this thread resolves: slot slot0 + tid
+    const __nv_bfloat16 *ksrc = nullptr, *vsrc = nullptr;
+    {
+        const int slot = slot0 + tid;
+        if (slot < a.topk) {
+            const int cntb = a.cnt ? min(max(a.cnt[b], 0), a.topk) : a.topk;
+            const int32_t e = slot < cntb ? a.idx[(int64_t)b * a.topk + slot] : -1;
+            if (e >= E) raise_flag(FLAG_ATTN_INDEX);
+            if (e >= 0 && e < E) {
+                ksrc = a.kc + (int64_t)b * a.c_sb + (int64_t)e * a.c_se;
+                vsrc = a.vc + (int64_t)b * a.c_sb + (int64_t)e * a.c_se;
+            }
+        } else if (slot < a.topk + a.window) {
+            const int64_t t = p - a.window + 1 + (slot - a.topk);
+            if (t >= 0 && t <= p) {
+                if (t >= a.N_cap) raise_flag(FLAG_ATTN_RANGE);
+                else {
+                    ksrc = a.k_raw + (int64_t)b * a.r_sb + t * a.r_st;
+                    vsrc = a.v_raw + (int64_t)b * a.r_sb + t * a.r_st;
+                }
+            }
+        }
+    }
+    const uint32_t bits = __ballot_sync(0xffffffffu, ksrc != nullptr);
+    if (lane == 0) s_mask[warp] = bits;
+    // ---- K rows (cp.async group 1), then V rows (group 2; empty when K and V are one
+    // buffer): a half-warp copies one 256-byte row, the row pointer comes by shuffle
+    // from the thread that resolved it
+    auto gather = [&](unsigned char *dst, const __nv_bfloat16 *src) {
+        const unsigned long long sv = reinterpret_cast<unsigned long long>(src);
+        const int c = lane & 15;
+#pragma unroll 4
+        for (int i = 0; i < 16; ++i) {
+            const int rl = 2 * i + (lane >> 4);
+            const unsigned long long rs = __shfl_sync(0xffffffffu, sv, rl);
+            const int r = warp * 32 + rl;
+            const __nv_bfloat16 *rp = reinterpret_cast<const __nv_bfloat16 *>(rs);
+            cp_async_16(smem_u32(dst + sw_off(r, c, kTBlk)), rp ? (const void *)(rp + c * 8) : (const void *)a.q,
+                        rp ? 16 : 0);  // zero-fill invalid rows
+        }
+    };
+    gather(sK, ksrc);
+    cp_async_commit();
+    if (!a.shared_kv) gather(sV, vsrc);
+    cp_async_commit();
+    const unsigned char *tV = a.shared_kv ? sK : sV;
+
+    // ---- S = Q K^T once Q and every thread's K rows have landed
+    cp_async_wait<1>();
+    tc::fence_proxy_async();
+    tc::fence_before();
+    __syncthreads();
+    tc::fence_after();
+    const uint32_t tmem = s_tmem;
+    const uint32_t tS = tmem, tO = tmem + kN;
+    if (tid == 0) {
+        constexpr uint32_t idS = tc::idesc_bf16(kH, kN, false, false);
+        const uint32_t aQ = smem_u32(sQ), aK = smem_u32(sK);
+#pragma unroll
+        for (int kk = 0; kk < kD / 16; ++kk) {
+            const uint64_t da = tc::desc_sw128(aQ + (kk >> 2) * kQBlk + (kk & 3) * 32, 16, 1024);
+            const uint64_t db = tc::desc_sw128(aK + (kk >> 2) * kTBlk + (kk & 3) * 32, 16, 1024);
+            tc::mma_bf16(tS, da, db, idS, kk > 0 ? 1u : 0u);
+        }
+        tc::commit(&bar_s);
+    }
+    cp_async_wait<0>();  // this thread's V rows
+    tc::fence_proxy_async();
+
+    // ---- softmax of the tile: thread (warp w, lane l < 16) owns head h = 16w + l
+    bool ok = wait_phase0(&bar_s);
+    ok = __syncthreads_and(ok) != 0;  // every thread's V rows, and S, or a give-up
+    if (!ok && tid == 0) raise_flag(FLAG_ATTN_RANGE | 0x800u);
+    tc::fence_after();
+    const bool active = lane < 16;
+    const int h = warp * 16 + lane;
+    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    float m_tile = -INFINITY, l_tile = 0.f;
+    if (ok) {
+        uint32_t v[kN];
+#pragma unroll
+        for (int c = 0; c < kN / 32; ++c) tc::tmem_ld32(tS + lane_off + c * 32, v + c * 32);
+        tc::tmem_wait_ld();
+        uint32_t mw[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) mw[q] = s_mask[q];
+        if ((mw[0] & mw[1] & mw[2] & mw[3]) != 0xffffffffu) {
+#pragma unroll
+            for (int c = 0; c < kN; ++c)
+                if (!((mw[c >> 5] >> (c & 31)) & 1u)) v[c] = __float_as_uint(-INFINITY);
+        }
+        float mx8[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) mx8[q] = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < kN; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], __uint_as_float(v[c]));
+        const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                               fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+        m_tile = mx == -INFINITY ? -INFINITY : mx * a.scale_log2;
+        const float nm = m_tile == -INFINITY ? 0.f : -m_tile;
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        // P = 2^(s * scale_log2 - m) in bf16 (invalid items read -inf: exponent 0)
+#pragma unroll
+        for (int cc = 0; cc < kN / 8; ++cc) {
+            uint32_t pk[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int c0 = cc * 8 + 2 * e;
+                const float p0 = tc::ex2(fmaf(__uint_as_float(v[c0]), a.scale_log2, nm));
+                const float p1 = tc::ex2(fmaf(__uint_as_float(v[c0 + 1]), a.scale_log2, nm));
+                acc[e] += p0 + p1;
+                pk[e] = pack_bf16x2(p0, p1);
+            }
+            if (active)
+                *reinterpret_cast<uint4 *>(sP + sw_off(h, cc, kQBlk)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        }
+        l_tile = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+    }
+    // ---- O = P V once every head's P row is in shared memory
+    tc::fence_proxy_async();
+    tc::fence_before();
+    __syncthreads();
+    tc::fence_after();
+    if (tid == 0 && ok) {
+        constexpr uint32_t idO = tc::idesc_bf16(kH, kD, false, true);
+        const uint32_t aP = smem_u32(sP), aV = smem_u32(tV);
+#pragma unroll
+        for (int kk = 0; kk < kN / 16; ++kk) {
+            const uint64_t da = tc::desc_sw128(aP + (kk >> 2) * kQBlk + (kk & 3) * 32, 16, 1024);
+            const uint64_t db = tc::desc_sw128(aV + kk * 16 * 128, kTBlk, 1024);
+            tc::mma_bf16(tO, da, db, idO, kk > 0 ? 1u : 0u);
+        }
+        tc::commit(&bar_o);
+    }
+    bool ok_o = ok ? wait_phase0(&bar_o) : false;
+    ok_o = __syncthreads_and(ok_o) != 0;
+    if (ok && !ok_o && tid == 0) raise_flag(FLAG_ATTN_RANGE | 0x800u);
+    tc::fence_after();
+    // ---- this CTA's partial: unnormalised O (over the K tile, free now), maximum, sum
+    if (ok_o) {
+#pragma unroll
+        for (int c = 0; c < kD / 32; ++c) {
+            uint32_t o[32];
+            tc::tmem_ld32(tO + lane_off + c * 32, o);
+            tc::tmem_wait_ld();
+            if (active) {
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    *reinterpret_cast<float4 *>(sO + o_off(h, c * 8 + e)) =
+                        make_float4(__uint_as_float(o[4 * e]), __uint_as_float(o[4 * e + 1]),
+                                    __uint_as_float(o[4 * e + 2]), __uint_as_float(o[4 * e + 3]));
+            }
+        }
+    }
+    if (active) {
+        sM[h] = ok_o ? m_tile : -INFINITY;  // a CTA that gave up contributes nothing
+        sL[h] = ok_o ? l_tile : 0.f;
+    }
+    cluster_sync_all();
+
+    // ---- combine heads [j * hpc, (j + 1) * hpc) over the n_tiles partials (DSMEM);
+    // all remote loads of a thread are issued before any is used
+    const int S = a.n_tiles;
+    const int hpc = (kH + S - 1) / S;
+    const int h_lo = j * hpc, h_hi = min(kH, h_lo + hpc);
+    const int work = h_hi > h_lo ? (h_hi - h_lo) * (kD / 4) : 0;
+    const uint32_t o_base = smem_u32(sO), m_base = smem_u32(sM), l_base = smem_u32(sL);
+    for (int w = tid; w < work; w += kThreads) {
+        const int hl = h_lo + w / (kD / 4), c4 = w % (kD / 4);
+        float mv[kMaxTiles], lv[kMaxTiles];
+        float4 ov[kMaxTiles];
+#pragma unroll
+        for (int r = 0; r < kMaxTiles; ++r) {
+            if (r < S) {
+                mv[r] = ld_dsmem_f32(map_rank(m_base + hl * 4, r));
+                lv[r] = ld_dsmem_f32(map_rank(l_base + hl * 4, r));
+                ov[r] = ld_dsmem_f32x4(map_rank(o_base + o_off(hl, c4) * 4, r));
+            } else {
+                mv[r] = -INFINITY;
+            }
+        }
+        float M = -INFINITY;
+#pragma unroll
+        for (int r = 0; r < kMaxTiles; ++r) M = fmaxf(M, mv[r]);
+        float Lsum = 0.f;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (M != -INFINITY) {
+#pragma unroll
+            for (int r = 0; r < kMaxTiles; ++r) {
+                if (mv[r] == -INFINITY) continue;  // nothing valid there (its O is not read)
+                const float wgt = tc::ex2(mv[r] - M);
+                Lsum = fmaf(wgt, lv[r], Lsum);
+                acc.x = fmaf(wgt, ov[r].x, acc.x);
+                acc.y = fmaf(wgt, ov[r].y, acc.y);
+                acc.z = fmaf(wgt, ov[r].z, acc.z);
+                acc.w = fmaf(wgt, ov[r].w, acc.w);
+            }
+        }
+        const bool empty = !(Lsum > 0.f);
+        const float inv = empty ? 0.f : 1.f / Lsum;
+        const int hh = hg * kH + hl;
+        __nv_bfloat16 *out = a.out + ((int64_t)b * a.H + hh) * kD + c4 * 4;
+        uint2 pk;
+        pk.x = pack_bf16x2(acc.x * inv, acc.y * inv);
+        pk.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+        *reinterpret_cast<uint2 *>(out) = pk;
+        if (a.lse && c4 == 0) a.lse[(int64_t)b * a.H + hh] = empty ? -INFINITY : (M + log2f(Lsum)) * kLn2;
+    }
+    cluster_sync_all();  // partials stay readable until every CTA of the cluster is done
+    // after a give-up, let this CTA's MMAs finish (again bounded) before TMEM is freed
+    if (tid == 0 && !ok) wait_phase0(&bar_s);
+    if (tid == 0 && ok && !ok_o) wait_phase0(&bar_o);
+    tc::fence_before();
+    __syncthreads();
+    tc::fence_after();
+    if (warp == 0) tc::tmem_dealloc(tmem, 256);
+}
+
+}  // namespace
+
+bool decode_tc_supported(const AttnArgs &a) {
+    return a.d == kD && a.H % kH == 0 && a.H > 0 && a.idx != nullptr && a.topk > 0 && a.T == 1 &&
+           a.pos_is_ctx && a.topk + a.window <= kMaxTiles * kN;
+}
+
+cudaError_t launch_attn_decode_tc(const AttnArgs &a, cudaStream_t s) {
+    DecodeTcArgs g;
+    g.B = a.rows;
+    g.H = a.H;
+    g.topk = a.topk;
+    g.window = a.window;
+    g.m = a.m;
+    g.n_tiles = (a.topk + a.window + kN - 1) / kN;
+    g.shared_kv = a.shared_kv;
+    g.E_cap = a.E_cap;
+    g.N_cap = a.N_cap;
+    g.c_sb = a.c_sb;
+    g.c_se = a.c_se;
+    g.r_sb = a.r_sb;
+    g.r_st = a.r_st;
+    g.ctx = a.pos;
+    g.idx = a.idx;
+    g.cnt = a.cnt;
+    g.q = static_cast<const __nv_bfloat16 *>(a.q);
+    g.kc = static_cast<const __nv_bfloat16 *>(a.kc);
+    g.vc = static_cast<const __nv_bfloat16 *>(a.vc);
+    g.k_raw = static_cast<const __nv_bfloat16 *>(a.k_raw);
+    g.v_raw = static_cast<const __nv_bfloat16 *>(a.v_raw);
+    g.scale_log2 = a.scale * kLog2e;
+    g.out = static_cast<__nv_bfloat16 *>(a.out);
+    g.lse = a.lse;
+    static unsigned long long done = 0, np_done = 0;
+    cudaError_t e = smem_limit_once(attn_decode_tc_kernel, (int)kSmemBytes, done);
+    if (e != cudaSuccess) return e;
+    if (g.n_tiles > 8) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        const unsigned long long bit = 1ull << (dev & 63);
+        if (!(np_done & bit)) {
+            e = cudaFuncSetAttribute(attn_decode_tc_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+            if (e != cudaSuccess) return e;
+            np_done |= bit;
+        }
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(g.n_tiles, a.rows, a.H / kH);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = g.n_tiles;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    // the launch may overlap the tail of the previous kernel in the stream; tiles that
+    // read the indexer's output wait for that kernel's completion first
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, attn_decode_tc_kernel, g);
+}
+
+}  // namespace hsa

@@ -386,7 +386,10 @@ hsa_status_t hsa_attn_decode(const void *q, hsa_dtype_t dt, int B, int H, int d,
     a.part_o = p.total ? reinterpret_cast<float *>(static_cast<char *>(ws) + p.off_o) : nullptr;
     a.part_lse = p.total ? reinterpret_cast<float *>(static_cast<char *>(ws) + p.off_lse) : nullptr;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (p.split < 0) return launched(hsa::launch_attn_decode_cluster(a, s), "attn_decode (cluster)");
+    if (p.split < 0) {
+        if (hsa::decode_tc_supported(a)) return launched(hsa::launch_attn_decode_tc(a, s), "attn_decode (tcgen05)");
+        return launched(hsa::launch_attn_decode_cluster(a, s), "attn_decode (cluster)");
+    }
     cudaError_t e = dt == HSA_BF16 ? hsa::launch_attn_bf16(a, s) : hsa::launch_attn_f32(a, s);
     if (e != cudaSuccess) return launched(e, "attn_decode");
     return launched(hsa::launch_attn_merge(a, dt == HSA_BF16, s), "attn_merge");
@@ -499,7 +502,7 @@ extern "C" hsa_status_t hsa_index_topk_noalloc(const int8_t *q_idx, int64_t q_sb
     if ((st = noalloc_scratch(&ws)) != HSA_OK) return st;
     if ((st = pending_error()) != HSA_OK) return st;
     // the array keeps the previous call's contents: zero what this call's kernels expect zeroed
-    cudaError_t e = cudaMemsetAsync(ws, 0, ch.bytes, s);
+    cudaError_t e = cudaMemsetAsync(ws, 0, ch.fused ? ch.fp.zero_bytes : ch.bytes, s);
     if (e != cudaSuccess) return launched(e, "index_topk_noalloc (clear scratch)");
     if (ch.fused) return launched(hsa::launch_index_fused(a, ch.fp, ws, s), "index_topk_noalloc (fused)");
     if (ch.prefill) return launched(hsa::launch_index_prefill(a, ch.pp, ws, di.num_sms, s), "index_topk_noalloc (tensor cores)");

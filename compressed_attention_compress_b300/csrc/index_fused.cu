@@ -543,6 +543,7 @@ FusedIndexPlan plan_index_fused(int rows, int DI, int64_t E_cap, int num_sms) {
     p.off_bar = off;
     off = align256(off + sizeof(unsigned) * 4 * (size_t)rows);
     p.off_rec = off;
+    p.zero_bytes = off;
     off = align256(off + sizeof(int) * (size_t)p.ctas_per_row * rows);
     p.off_cand = off;
     off = align256(off + sizeof(uint2) * (size_t)p.ctas_per_row * p.chunk * rows);

@@ -78,6 +78,7 @@ struct FusedIndexPlan {
     int off_stage_smem;  // byte offset of the copy stages in dynamic shared memory
     size_t smem;
     size_t off_hist1, off_bar, off_rec, off_cand, total;
+    size_t zero_bytes;   // the leading part that must be zero before a launch (histograms, counters)
 };
 FusedIndexPlan plan_index_fused(int rows, int DI, int64_t E_cap, int num_sms);
 cudaError_t launch_index_fused(const IndexArgs &a, const FusedIndexPlan &p, void *ws, cudaStream_t s);
@@ -181,6 +182,10 @@ cudaError_t launch_attn_merge(const AttnArgs &a, bool bf16, cudaStream_t s);
 // bf16 decode with H in {16, 32, 64, 128}: one cluster per sequence, no workspace.
 bool decode_cluster_supported(int H, int d);
 cudaError_t launch_attn_decode_cluster(const AttnArgs &a, cudaStream_t s);
+// bf16 CSA decode with d = 128, H a multiple of 64, topk + window <= 2048: one
+// cluster of 128-item tiles per (sequence, 64-head group), tcgen05 MMAs.
+bool decode_tc_supported(const AttnArgs &a);
+cudaError_t launch_attn_decode_tc(const AttnArgs &a, cudaStream_t s);
 // bf16 dense (HCA) prefill with d = 128 and T*H a multiple of 128: tcgen05 + TMA kernel.
 bool prefill_tc_supported(const AttnArgs &a);
 cudaError_t launch_attn_prefill_tc(const AttnArgs &a, int num_sms, cudaStream_t s);

@@ -218,9 +218,10 @@ def test_attn_decode_without_cnt_and_unsorted_idx(lib):
     assert_close_out(out, ro, torch.bfloat16)
 
 
-def test_attn_decode_window_only_and_empty(lib):
+@pytest.mark.parametrize("H", [16, 64])
+def test_attn_decode_window_only_and_empty(lib, H):
     # k = 0 (all -1) -> sliding-window attention; window 0 + no entries -> empty set
-    B, H, d, m = 2, 16, 128, 4
+    B, d, m = 2, 128, 4
     N = 500
     kc, vc, kr, vr = _attn_inputs(B, N // m, N, H, d, torch.bfloat16, 60)
     q = _randn((B, H, d), 64)
