@@ -16,10 +16,12 @@
 //     (h / 16) * 32 + h % 16, so lanes 0-15 of warp w hold heads 16w..16w+15);
 //   - takes the masked softmax of its tile, one head per thread, writes P (bf16)
 //     to shared memory and accumulates O = P V into TMEM;
-//   - keeps its unnormalised partial (O, maximum, sum) in shared memory.
-// After a cluster barrier CTA r combines heads [r * hpc, (r + 1) * hpc) of all the
-// partials through distributed shared memory with the log-sum-exp rule and writes
-// the output and the log-sum-exp.  Q, the TMEM allocation and tiles that hold only
+//   - writes its unnormalised partial (O, maximum, sum) to the workspace with
+//     coalesced stores.
+// After a cluster barrier (its release/acquire also orders these global writes for
+// the cluster) CTA r reads heads [r * hpc, (r + 1) * hpc) of all the partials from
+// L2, combines them with the log-sum-exp rule and writes the output and the
+// log-sum-exp.  Q, the TMEM allocation and tiles that hold only
 // window tokens need nothing from the indexer, so they run before the kernel waits
 // for the preceding grid (the launch uses programmatic stream serialization).
 // Every wait is bounded; a wait that gives up raises the device flag, and the CTA
@@ -58,14 +60,16 @@ struct DecodeTcArgs {
     float scale_log2;
     __nv_bfloat16 *out;          // [B, H, d]
     float *lse;                  // [B, H] or null
+    float *part_o;               // [B, H / 64, n_tiles, 64, d] fp32 partial O
+    float *part_ml;              // [B, H / 64, n_tiles, 2, 64]: maximum (log2 units), sum
 };
 
 // chunk c (16 bytes) of row r of a 128-byte-swizzled K-major tile made of 64-column blocks
 __device__ __forceinline__ uint32_t sw_off(int r, int c, int blk_bytes) {
     return (uint32_t)((c >> 3) * blk_bytes + r * 128 + (((c & 7) ^ (r & 7)) << 4));
 }
-// float4 chunk c4 of row h of the fp32 partial O, rotated so that the 16 heads a
-// warp stores at once spread over the banks
+// float4 chunk c4 of row h of the fp32 partial O staged in shared memory, rotated so
+// that the 16 heads a warp stores at once spread over the banks
 __device__ __forceinline__ int o_off(int h, int c4) { return h * kD + ((c4 ^ (h & 31)) << 2); }
 
 __device__ __forceinline__ bool wait_phase0(uint64_t *bar) {
@@ -82,7 +86,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_tc_kernel(DecodeTcArg
     unsigned char *sV = sK + kTile;
     unsigned char *sP = sV + kTile;
     float *sO = reinterpret_cast<float *>(sK);
-    __shared__ float sM[kH], sL[kH];
     __shared__ uint32_t s_mask[kThreads / 32];
     __shared__ __align__(8) uint64_t bar_s, bar_o;
     __shared__ uint32_t s_tmem;
@@ -251,45 +254,54 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_tc_kernel(DecodeTcArg
     ok_o = __syncthreads_and(ok_o) != 0;
     if (ok && !ok_o && tid == 0) raise_flag(FLAG_ATTN_RANGE | 0x800u);
     tc::fence_after();
-    // ---- this CTA's partial: unnormalised O (over the K tile, free now), maximum, sum
+    // ---- this CTA's partial: unnormalised O, staged in the K tile (free now) and
+    // written to the workspace with coalesced stores, maximum and sum
+    const int S = a.n_tiles;
+    const int64_t blk = ((int64_t)b * (a.H / kH) + hg) * S;  // partials of (sequence, head group)
     if (ok_o) {
+        uint32_t o[kD];
 #pragma unroll
-        for (int c = 0; c < kD / 32; ++c) {
-            uint32_t o[32];
-            tc::tmem_ld32(tO + lane_off + c * 32, o);
-            tc::tmem_wait_ld();
-            if (active) {
+        for (int c = 0; c < kD / 32; ++c) tc::tmem_ld32(tO + lane_off + c * 32, o + c * 32);
+        tc::tmem_wait_ld();
+        if (active) {
 #pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    *reinterpret_cast<float4 *>(sO + o_off(h, c * 8 + e)) =
-                        make_float4(__uint_as_float(o[4 * e]), __uint_as_float(o[4 * e + 1]),
-                                    __uint_as_float(o[4 * e + 2]), __uint_as_float(o[4 * e + 3]));
-            }
+            for (int c4 = 0; c4 < kD / 4; ++c4)
+                *reinterpret_cast<float4 *>(sO + o_off(h, c4)) =
+                    make_float4(__uint_as_float(o[4 * c4]), __uint_as_float(o[4 * c4 + 1]),
+                                __uint_as_float(o[4 * c4 + 2]), __uint_as_float(o[4 * c4 + 3]));
         }
     }
-    if (active) {
-        sM[h] = ok_o ? m_tile : -INFINITY;  // a CTA that gave up contributes nothing
-        sL[h] = ok_o ? l_tile : 0.f;
+    if (active) {  // a CTA that gave up contributes nothing (its O is never read)
+        float *pml = a.part_ml + (blk + j) * (2 * kH);
+        pml[h] = ok_o ? m_tile : -INFINITY;
+        pml[kH + h] = ok_o ? l_tile : 0.f;
     }
-    cluster_sync_all();
+    __syncthreads();
+    if (ok_o) {
+        float *po = a.part_o + (blk + j) * (kH * kD);
+        for (int hr = warp; hr < kH; hr += kThreads / 32)  // warp w: rows w, w + 4, ...; lane: chunk
+            *reinterpret_cast<float4 *>(po + hr * kD + lane * 4) =
+                *reinterpret_cast<const float4 *>(sO + o_off(hr, lane));
+    }
+    cluster_sync_all();  // every partial of the cluster is written
 
-    // ---- combine heads [j * hpc, (j + 1) * hpc) over the n_tiles partials (DSMEM);
-    // all remote loads of a thread are issued before any is used
-    const int S = a.n_tiles;
+    // ---- combine heads [j * hpc, (j + 1) * hpc) over the n_tiles partials (from L2);
+    // all loads of a thread are issued before any is used
     const int hpc = (kH + S - 1) / S;
     const int h_lo = j * hpc, h_hi = min(kH, h_lo + hpc);
     const int work = h_hi > h_lo ? (h_hi - h_lo) * (kD / 4) : 0;
-    const uint32_t o_base = smem_u32(sO), m_base = smem_u32(sM), l_base = smem_u32(sL);
     for (int w = tid; w < work; w += kThreads) {
-        const int hl = h_lo + w / (kD / 4), c4 = w % (kD / 4);
+        const int hl = h_lo + w / (kD / 4);  // head within the group
+        const int c4 = w % (kD / 4);
         float mv[kMaxTiles], lv[kMaxTiles];
         float4 ov[kMaxTiles];
 #pragma unroll
         for (int r = 0; r < kMaxTiles; ++r) {
             if (r < S) {
-                mv[r] = ld_dsmem_f32(map_rank(m_base + hl * 4, r));
-                lv[r] = ld_dsmem_f32(map_rank(l_base + hl * 4, r));
-                ov[r] = ld_dsmem_f32x4(map_rank(o_base + o_off(hl, c4) * 4, r));
+                const float *pml = a.part_ml + (blk + r) * (2 * kH);
+                mv[r] = __ldcg(pml + hl);
+                lv[r] = __ldcg(pml + kH + hl);
+                ov[r] = __ldcg(reinterpret_cast<const float4 *>(a.part_o + (blk + r) * (kH * kD) + hl * kD) + c4);
             } else {
                 mv[r] = -INFINITY;
             }
@@ -321,7 +333,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_tc_kernel(DecodeTcArg
         *reinterpret_cast<uint2 *>(out) = pk;
         if (a.lse && c4 == 0) a.lse[(int64_t)b * a.H + hh] = empty ? -INFINITY : (M + log2f(Lsum)) * kLn2;
     }
-    cluster_sync_all();  // partials stay readable until every CTA of the cluster is done
     // after a give-up, let this CTA's MMAs finish (again bounded) before TMEM is freed
     if (tid == 0 && !ok) wait_phase0(&bar_s);
     if (tid == 0 && ok && !ok_o) wait_phase0(&bar_o);
@@ -333,9 +344,22 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_tc_kernel(DecodeTcArg
 
 }  // namespace
 
+bool decode_tc_shape(int H, int d, int topk, int window) {
+    return d == kD && H > 0 && H % kH == 0 && topk > 0 && window >= 0 && topk + window <= kMaxTiles * kN;
+}
+
+DecodeTcWorkspace decode_tc_workspace(int B, int H, int topk, int window) {
+    DecodeTcWorkspace w;
+    const size_t parts = (size_t)B * (H / kH) * ((topk + window + kN - 1) / kN);
+    w.off_o = 0;
+    w.off_ml = (parts * kH * kD * sizeof(float) + 255) & ~(size_t)255;
+    w.total = w.off_ml + ((parts * 2 * kH * sizeof(float) + 255) & ~(size_t)255);
+    return w;
+}
+
 bool decode_tc_supported(const AttnArgs &a) {
-    return a.d == kD && a.H % kH == 0 && a.H > 0 && a.idx != nullptr && a.topk > 0 && a.T == 1 &&
-           a.pos_is_ctx && a.topk + a.window <= kMaxTiles * kN;
+    return decode_tc_shape(a.H, a.d, a.topk, a.window) && a.idx != nullptr && a.T == 1 && a.pos_is_ctx &&
+           a.part_o != nullptr && a.part_lse != nullptr;
 }
 
 cudaError_t launch_attn_decode_tc(const AttnArgs &a, cudaStream_t s) {
@@ -364,6 +388,8 @@ cudaError_t launch_attn_decode_tc(const AttnArgs &a, cudaStream_t s) {
     g.scale_log2 = a.scale * kLog2e;
     g.out = static_cast<__nv_bfloat16 *>(a.out);
     g.lse = a.lse;
+    g.part_o = a.part_o;
+    g.part_ml = a.part_lse;
     static unsigned long long done = 0, np_done = 0;
     cudaError_t e = smem_limit_once(attn_decode_tc_kernel, (int)kSmemBytes, done);
     if (e != cudaSuccess) return e;

@@ -95,6 +95,16 @@ DecodePlan plan_decode(hsa_dtype_t dt, int B, int H, int d, int64_t E_cap, int m
                        bool dense, int num_sms) {
     DecodePlan p{};
     (void)m;
+    if (dt == HSA_BF16 && !dense && hsa::decode_tc_shape(H, d, topk, window)) {
+        // tcgen05 kernel: one cluster per (sequence, head group), partials in the workspace
+        const hsa::DecodeTcWorkspace w = hsa::decode_tc_workspace(B, H, topk, window);
+        p.split = -1;
+        p.max_splits = 1;
+        p.off_o = w.off_o;
+        p.off_lse = w.off_ml;
+        p.total = w.total;
+        return p;
+    }
     if (dt == HSA_BF16 && hsa::decode_cluster_supported(H, d)) {
         p.split = -1;  // cluster kernel: splits live in one cluster, no workspace
         p.max_splits = 1;

@@ -182,8 +182,14 @@ cudaError_t launch_attn_merge(const AttnArgs &a, bool bf16, cudaStream_t s);
 // bf16 decode with H in {16, 32, 64, 128}: one cluster per sequence, no workspace.
 bool decode_cluster_supported(int H, int d);
 cudaError_t launch_attn_decode_cluster(const AttnArgs &a, cudaStream_t s);
-// bf16 CSA decode with d = 128, H a multiple of 64, topk + window <= 2048: one
-// cluster of 128-item tiles per (sequence, 64-head group), tcgen05 MMAs.
+// bf16 CSA decode with d = 128, H a multiple of 64, 0 < topk, topk + window <= 2048:
+// one cluster of 128-item tiles per (sequence, 64-head group), tcgen05 MMAs; the
+// tiles' partials go through a workspace (part_o: O, part_lse: maximum and sum).
+bool decode_tc_shape(int H, int d, int topk, int window);
+struct DecodeTcWorkspace {
+    size_t off_o, off_ml, total;
+};
+DecodeTcWorkspace decode_tc_workspace(int B, int H, int topk, int window);
 bool decode_tc_supported(const AttnArgs &a);
 cudaError_t launch_attn_decode_tc(const AttnArgs &a, cudaStream_t s);
 // bf16 dense (HCA) prefill with d = 128 and T*H a multiple of 128: tcgen05 + TMA kernel.

@@ -271,8 +271,9 @@ def test_attn_prefill_parity(lib, dtype, H, d, dense):
 
 # ---------------------------------------------------------- error paths ---
 
-def test_errors_leave_stream_usable(lib):
-    B, H, d, m, W = 1, 16, 128, 4, 16
+@pytest.mark.parametrize("H", [16, 64])
+def test_errors_leave_stream_usable(lib, H):
+    B, d, m, W = 1, 128, 4, 16
     N = 256
     kc, vc, kr, vr = [t.cuda() for t in _attn_inputs(B, N // m, N, H, d, torch.bfloat16, 80)]
     q = _randn((B, H, d), 84).cuda()
