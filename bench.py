@@ -44,12 +44,12 @@ WL = WORKLOADS["pro_csa_decode"]
 # ncu capture summarised in profiles/index_fused_kernel_pro_csa_1M_B4.md; reported only
 # while the kernel's sources are the ones that capture ran.
 INDEX_TRAFFIC = {
-    "bytes": 67210240 + 207104,
+    "bytes": 67258368 + 110336,
     "sources": {
         "compressed_attention_compress_b300/csrc/index_fused.cu":
-            "45fab5ff0d11b0d0993b7e1caaa948ba9600dabb8db8f34c338c31e2c604dade",
+            "fd9e0083f6ed2eebb211bcb3ff11a3142598ba316ffa91176b925dcc9d2cf824",
         "compressed_attention_compress_b300/csrc/common.cuh":
-            "35428b34db55a12ea4c19016f4b5a1d3dbe35eca7162b0449b366e789980467b",
+            "1c50e4616466d69022320548d2a47c9c9d2aef65c6b5dca650519a168e3275b2",
         "compressed_attention_compress_b300/csrc/block_scan.cuh":
             "ac0c74255584e15eaea3aa69860c5b08cd4267e432e4e9db82d6c3de8245161a",
     },
