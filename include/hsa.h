@@ -243,7 +243,14 @@ HSA_API hsa_status_t hsa_index_topk_noalloc(const int8_t *q_idx, int64_t q_sb, i
  *   k_raw, v_raw [B, N_cap, d] of `dt`, strides (r_sb, r_st)
  *   ctx_len    device int64 [B]; 1 <= ctx_len <= N_cap
  *   out        [B, H, d] of `dt`, contiguous;  lse fp32 [B, H] or NULL
- *   ws         workspace of hsa_attn_decode_workspace_size bytes
+ *   ws         workspace of hsa_attn_decode_workspace_size bytes (may be 0):
+ *              the parts' partial results.  For bf16 CSA with d = 128, H a
+ *              multiple of 64 and topk + window <= 2048 the parts are tiles of
+ *              128 slots, one thread-block cluster per (sequence, 64 heads), and
+ *              the workspace holds their fp32 partials, about B * H/64 *
+ *              ceil((topk + window) / 128) * 33,280 bytes.
+ * Every pointer is a device pointer (memory the GPU can address); host memory,
+ * pinned or not, is not accepted.
  * bf16: d in {64, 128}, H a multiple of 16 up to 128.  fp32: d a multiple of
  * 32 up to 256, any H.
  */
