@@ -10,9 +10,10 @@
 // an M = 64 (heads) problem: S = Q K_j^T (N = 128 items per tile, K = d = 128) and
 // O += P V_j, with S and O in TMEM (row h of an M = 64 accumulator lives in TMEM
 // lane (h / 16) * 32 + h % 16).  One persistent CTA per SM walks tokens:
-//   warps 0-3  softmax, one head per thread (lanes 0-15 of each warp): S from TMEM,
-//              masked maximum, exponents, P (bf16) into shared memory for the
-//              second MMA, O rescaled in TMEM only when the maximum grows by > 2^8.
+//   warps 0-3  softmax, two lanes per head (lane l < 16 and l + 16 of warp w take
+//              halves of head 16w + l's row): S from TMEM into registers, masked
+//              maximum, exponents, P (bf16) into shared memory for the second MMA,
+//              O rescaled in TMEM only when the maximum grows by > 2^8.
 //   warps 4-7  gather: each thread resolves one item row of tile j (selected entry
 //              of Kc/Vc or window token of the raw cache, zero-filled when
 //              invalid); half-warps then copy whole 256-byte rows with 16-byte
@@ -309,6 +310,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---------------------------------------------------------------- softmax
         const bool active = lane < 16;
         const int h = warp * 16 + lane;  // head of this thread (active lanes)
+        const bool upper = lane >= 16;
+        const int hr = warp * 16 + (lane & 15);  // the head whose row this lane works on
         const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
         int64_t g = 0;
         int it = 0;
@@ -326,33 +329,44 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int q = 0; q < 4; ++q) mw[q] = s_mask[ms][q];
                 arrive(&bars.m_empty[ms]);
-                // pass 1: masked raw maximum over S, 64 columns at a time (eight chains);
+                // S of this tile into registers, two lanes per head: lane l < 16 takes
+                // columns 0-63 of head h's row (TMEM lane 32w + l), lane l + 16 columns
+                // 64-127 of the same row, passed over by a shuffle; 32 columns per load.
+                // The S buffer is free for the next tile's MMA as soon as it is read.
+                uint32_t v[64];
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    uint32_t w[32];
+                    tc::tmem_ld32(tS[g & 1] + lane_off + 64 + q * 32, w);
+                    tc::tmem_wait_ld();
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) v[q * 32 + c] = __shfl_xor_sync(0xffffffffu, w[c], 16);
+                }
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    uint32_t w[32];
+                    tc::tmem_ld32(tS[g & 1] + lane_off + q * 32, w);
+                    tc::tmem_wait_ld();
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) v[q * 32 + c] = upper ? v[q * 32 + c] : w[c];
+                }
+                tc::fence_before();
+                arrive(&bars.s_free[g & 1]);  // S has been read in full
                 // tiles with every item valid (the common case) skip the mask
-                const bool all_valid = (mw[0] & mw[1] & mw[2] & mw[3]) == 0xffffffffu;
+                if ((mw[0] & mw[1] & mw[2] & mw[3]) != 0xffffffffu) {
+                    const uint32_t m0 = upper ? mw[2] : mw[0], m1 = upper ? mw[3] : mw[1];
+#pragma unroll
+                    for (int c = 0; c < 64; ++c)
+                        if (!(((c < 32 ? m0 : m1) >> (c & 31)) & 1u)) v[c] = __float_as_uint(-INFINITY);
+                }
                 float mx8[8];
 #pragma unroll
                 for (int q = 0; q < 8; ++q) mx8[q] = -INFINITY;
 #pragma unroll
-                for (int hf = 0; hf < 2; ++hf) {
-                    uint32_t v[64];
-                    tc::tmem_ld32(tS[g & 1] + lane_off + hf * 64, v);
-                    tc::tmem_ld32(tS[g & 1] + lane_off + hf * 64 + 32, v + 32);
-                    tc::tmem_wait_ld();
-                    if (all_valid) {
-#pragma unroll
-                        for (int c = 0; c < 64; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], __uint_as_float(v[c]));
-                    } else {
-                        const uint32_t w0 = mw[2 * hf], w1 = mw[2 * hf + 1];
-#pragma unroll
-                        for (int c = 0; c < 64; ++c) {
-                            const bool ok_c = ((c < 32 ? w0 : w1) >> (c & 31)) & 1u;
-                            mx8[c & 7] = fmaxf(mx8[c & 7], ok_c ? __uint_as_float(v[c]) : -INFINITY);
-                        }
-                    }
-                }
-                const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                                       fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) *
-                                 a.scale_log2;
+                for (int c = 0; c < 64; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], __uint_as_float(v[c]));
+                float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                                 fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16)) * a.scale_log2;
                 bool rescale = false;
                 float alpha = 1.f;
                 if (mx > m_used + kRescale) {
@@ -380,44 +394,29 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     tc::tmem_wait_st();
                 }
-                // pass 2: P = 2^(x * scale_log2 - m_used) in bf16, 128-byte-swizzled K-major rows;
-                // invalid items read as -inf (exponent 0), the scale goes into a packed FMA
+                // P = 2^(x * scale_log2 - m_used) in bf16, 128-byte-swizzled K-major rows (each
+                // lane its 64 columns); invalid items read as -inf (exponent 0), the scale goes
+                // into a packed FMA
                 const float nmu = m_used == -INFINITY ? 0.f : -m_used;
                 const uint64_t nmu2 = pack2(nmu, nmu), sc2 = pack2(a.scale_log2, a.scale_log2);
                 uint64_t acc2[4] = {0, 0, 0, 0};
 #pragma unroll
-                for (int hf = 0; hf < 2; ++hf) {
-                    uint32_t v[64];
-                    tc::tmem_ld32(tS[g & 1] + lane_off + hf * 64, v);
-                    tc::tmem_ld32(tS[g & 1] + lane_off + hf * 64 + 32, v + 32);
-                    tc::tmem_wait_ld();
-                    if (!all_valid) {
-                        const uint32_t w0 = mw[2 * hf], w1 = mw[2 * hf + 1];
+                for (int cc = 0; cc < 8; ++cc) {
+                    uint32_t pk[4];
 #pragma unroll
-                        for (int c = 0; c < 64; ++c)
-                            if (!(((c < 32 ? w0 : w1) >> (c & 31)) & 1u)) v[c] = __float_as_uint(-INFINITY);
+                    for (int e = 0; e < 4; ++e) {
+                        const int c0 = cc * 8 + 2 * e;
+                        const uint64_t arg = fma_f32x2(((uint64_t)v[c0 + 1] << 32) | v[c0], sc2, nmu2);
+                        const float p0 = tc::ex2(lo_of(arg)), p1 = tc::ex2(hi_of(arg));
+                        acc2[e] = add_f32x2(acc2[e], pack2(p0, p1));
+                        pk[e] = pack_bf16x2(p0, p1);
                     }
-                    if (active) {
-#pragma unroll
-                        for (int cc = 0; cc < 8; ++cc) {
-                            uint32_t pk[4];
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                const int c0 = cc * 8 + 2 * e;
-                                const uint64_t arg = fma_f32x2(((uint64_t)v[c0 + 1] << 32) | v[c0], sc2, nmu2);
-                                const float p0 = tc::ex2(lo_of(arg)), p1 = tc::ex2(hi_of(arg));
-                                acc2[e] = add_f32x2(acc2[e], pack2(p0, p1));
-                                pk[e] = pack_bf16x2(p0, p1);
-                            }
-                            *reinterpret_cast<uint4 *>(sP + hf * kQBlk + h * 128 + ((cc ^ (h & 7)) << 4)) =
-                                make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                        }
-                    }
+                    *reinterpret_cast<uint4 *>(sP + (upper ? kQBlk : 0) + hr * 128 + ((cc ^ (hr & 7)) << 4)) =
+                        make_uint4(pk[0], pk[1], pk[2], pk[3]);
                 }
                 const uint64_t s4 = add_f32x2(add_f32x2(acc2[0], acc2[1]), add_f32x2(acc2[2], acc2[3]));
-                const float sum = lo_of(s4) + hi_of(s4);
-                tc::fence_before();
-                arrive(&bars.s_free[g & 1]);  // S has been read in full
+                float sum = lo_of(s4) + hi_of(s4);
+                sum += __shfl_xor_sync(0xffffffffu, sum, 16);
                 l += sum;
                 tc::fence_proxy_async();
                 tc::fence_before();
