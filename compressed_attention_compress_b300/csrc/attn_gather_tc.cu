@@ -172,12 +172,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             ok = __all_sync(0xffffffffu, ok);  // the warp's lanes leave together (ballots below)
+            // selected indices are loaded one tile ahead, so each load's round trip overlaps
+            // the copies of the tile before
+            int32_t e_next = (gt < a.topk && gt < cntr) ? a.idx[(int64_t)row * a.topk + gt] : -1;
             for (int j = 0; j < nt && ok; ++j, ++g) {
                 // the item this thread copies, and whether it is valid
                 const int slot_i = j * kN + gt;
+                const int32_t e = e_next;
+                {
+                    const int slot_n = slot_i + kN;
+                    e_next = (slot_n < a.topk && slot_n < cntr) ? a.idx[(int64_t)row * a.topk + slot_n] : -1;
+                }
                 const __nv_bfloat16 *ksrc = nullptr, *vsrc = nullptr;
                 if (slot_i < a.topk) {
-                    const int32_t e = slot_i < cntr ? a.idx[(int64_t)row * a.topk + slot_i] : -1;
                     if (e >= E) raise_flag(FLAG_ATTN_INDEX);
                     if (e >= 0 && e < E) {
                         ksrc = a.kc + b * a.c_sb + (int64_t)e * a.c_se;
