@@ -25,7 +25,7 @@
 // window tokens need nothing from the indexer, so they run before the kernel waits
 // for the preceding grid (the launch uses programmatic stream serialization).
 // Every wait is bounded; a wait that gives up raises the device flag, and the CTA
-// still reaches both cluster barriers and frees its TMEM.
+// still reaches the cluster barrier and frees its TMEM.
 #include <math.h>
 
 #include "internal.h"
