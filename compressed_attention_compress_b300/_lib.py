@@ -22,7 +22,7 @@ _STATUS = {0: "HSA_OK", 1: "HSA_ERR_INVALID_ARG", 2: "HSA_ERR_UNSUPPORTED", 3: "
            4: "HSA_ERR_CUDA", 5: "HSA_ERR_DEVICE_FLAG"}
 
 # every symbol include/hsa.h declares
-EXPORTS = ["hsa_last_error", "hsa_version", "hsa_check", "hsa_compress", "hsa_compress_append", "hsa_compress_learned", "hsa_index_topk_workspace_size",
+EXPORTS = ["hsa_last_error", "hsa_version", "hsa_check", "hsa_check_pointer", "hsa_compress", "hsa_compress_append", "hsa_compress_learned", "hsa_index_topk_workspace_size",
            "hsa_index_topk", "hsa_index_topk_noalloc", "hsa_attn_decode_workspace_size", "hsa_attn_decode",
            "hsa_attn_prefill_workspace_size", "hsa_attn_prefill", "hsa_index_scores", "hsa_topk_merge",
            "hsa_lse_merge", "hsa_rmsnorm_rope", "hsa_attn_finalize"]
@@ -45,6 +45,8 @@ def _load():
     lib.hsa_version.restype = I
     lib.hsa_check.restype = I
     lib.hsa_check.argtypes = [P]
+    lib.hsa_check_pointer.restype = I
+    lib.hsa_check_pointer.argtypes = [P]
     lib.hsa_compress.restype = I
     lib.hsa_compress.argtypes = [P, P, I, I, I, I64, I64, I64, P, P, I64, P, I, P, P, I64, I64, I64, P]
     lib.hsa_compress_learned.restype = I
@@ -108,6 +110,11 @@ def _dt(t):
 
 def hsa_check(stream=None):
     _chk(lib.hsa_check(_stream(stream)))
+
+
+def hsa_check_pointer(ptr: int):
+    """Raise HSAError unless the address `ptr` is device memory of the current device (or managed)."""
+    _chk(lib.hsa_check_pointer(ctypes.c_void_p(ptr)))
 
 
 def hsa_compress(k, v, tok_begin, tok_end, max_blocks, w, m, kc, vc, stream=None):

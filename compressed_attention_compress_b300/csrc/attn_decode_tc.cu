@@ -21,9 +21,11 @@
 // After a cluster barrier (its release/acquire also orders these global writes for
 // the cluster) CTA r reads heads [r * hpc, (r + 1) * hpc) of all the partials from
 // L2, combines them with the log-sum-exp rule and writes the output and the
-// log-sum-exp.  Q, the TMEM allocation and tiles that hold only
-// window tokens need nothing from the indexer, so they run before the kernel waits
-// for the preceding grid (the launch uses programmatic stream serialization).
+// log-sum-exp.  The launch uses programmatic stream serialization: the barrier
+// set-up and the TMEM allocation overlap the tail of the preceding kernel, and
+// every CTA waits for that kernel's completion (griddepcontrol.wait) before it
+// reads any input, since that kernel may have written the query, the positions,
+// the cache or the selected indices.
 // Every wait is bounded; a wait that gives up raises the device flag, and the CTA
 // still reaches the cluster barrier and frees its TMEM.
 #include <math.h>
@@ -100,6 +102,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_tc_kernel(DecodeTcArg
         fence_mbar_init();
     }
     if (warp == 0) tc::tmem_alloc(&s_tmem, 256);  // S: columns [0, 128), O: [128, 256)
+    // nothing written by the preceding kernel in the stream is read before this
+    asm volatile("griddepcontrol.wait;\n" ::: "memory");
     // Q of this head group into 128-byte-swizzled K-major rows (cp.async group 0)
     {
         const __nv_bfloat16 *q = a.q + ((int64_t)b * a.H + (int64_t)hg * kH) * kD;
@@ -113,8 +117,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_tc_kernel(DecodeTcArg
     int64_t E = num_entries(p, a.m);
     if (E > a.E_cap) E = a.E_cap;
     const int slot0 = j * kN;
-    // the indexer's output (idx, cnt) is read only by tiles holding selected-entry slots
-    if (slot0 < a.topk) asm volatile("griddepcontrol.wait;\n" ::: "memory");
 
     // ---- the item this thread resolves: slot slot0 + tid
     const __nv_bfloat16 *ksrc = nullptr, *vsrc = nullptr;
@@ -413,8 +415,8 @@ cudaError_t launch_attn_decode_tc(const AttnArgs &a, cudaStream_t s) {
     attr[0].val.clusterDim.x = g.n_tiles;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
-    // the launch may overlap the tail of the previous kernel in the stream; tiles that
-    // read the indexer's output wait for that kernel's completion first
+    // the launch may overlap the tail of the previous kernel in the stream (set-up
+    // only: every CTA waits for that kernel's completion before reading inputs)
     attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;

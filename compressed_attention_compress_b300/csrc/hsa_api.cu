@@ -6,6 +6,7 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <initializer_list>
 #include <mutex>
 
 #include "../../include/hsa.h"
@@ -73,6 +74,47 @@ hsa_status_t launched(cudaError_t e, const char *what) {
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+// Every buffer must be memory the current device addresses directly: device
+// memory of this device or managed memory.  Host memory (pageable or pinned) and
+// another device's memory are refused on the host, before anything is enqueued,
+// so that a wrong pointer never reaches a kernel.  Null pointers are skipped here
+// (whether an argument may be null is checked by the caller).
+hsa_status_t check_pointer(const void *p, const char *what) {
+    if (!p) return HSA_OK;
+    cudaPointerAttributes at;
+    cudaError_t e = cudaPointerGetAttributes(&at, p);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(HSA_ERR_INVALID_ARG, "%s: not a CUDA-visible pointer (%s)", what, cudaGetErrorString(e));
+    }
+    if (at.type == cudaMemoryTypeManaged) return HSA_OK;
+    if (at.type != cudaMemoryTypeDevice)
+        return fail(HSA_ERR_INVALID_ARG, "%s: host memory (%s); pass device memory", what,
+                    at.type == cudaMemoryTypeHost ? "pinned" : "pageable");
+    int dev = 0;
+    e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail(HSA_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+    if (at.device != dev)
+        return fail(HSA_ERR_INVALID_ARG, "%s: memory of device %d, the current device is %d", what, at.device, dev);
+    return HSA_OK;
+}
+
+struct NamedPtr {
+    const void *p;
+    const char *what;
+};
+hsa_status_t check_pointers(std::initializer_list<NamedPtr> ptrs) {
+    for (const NamedPtr &x : ptrs) {
+        hsa_status_t st = check_pointer(x.p, x.what);
+        if (st != HSA_OK) return st;
+    }
+    return HSA_OK;
+}
+
+// Query rows (B * T) an indexer or attention call may take: the launch grids and
+// per-row workspace offsets are sized in int for at most this many rows.
+constexpr int64_t kMaxRows = 1ll << 24;
 size_t esize(hsa_dtype_t dt) { return dt == HSA_BF16 ? 2 : 4; }
 bool dtype_ok(hsa_dtype_t dt) { return dt == HSA_BF16 || dt == HSA_F32; }
 
@@ -153,7 +195,9 @@ hsa_status_t check_attn_common(const void *q, hsa_dtype_t dt, int B, int T, int 
     if (c_sb % vec || c_se % vec || r_sb % vec || r_st % vec)
         return fail(HSA_ERR_UNSUPPORTED, "cache strides must be multiples of 16 bytes");
     if (c_se < d || r_st < d || c_sb < 0 || r_sb < 0) return fail(HSA_ERR_INVALID_ARG, "cache strides overlap rows");
-    return HSA_OK;
+    if (B * (int64_t)T > kMaxRows) return fail(HSA_ERR_UNSUPPORTED, "B*T above 2^24");
+    return check_pointers({{q, "q"}, {kc, "kc"}, {vc, "vc"}, {idx, "idx"}, {k_raw, "k_raw"}, {v_raw, "v_raw"},
+                           {pos, "positions"}, {out, "out"}});
 }
 
 }  // namespace
@@ -162,7 +206,13 @@ extern "C" {
 
 const char *hsa_last_error(void) { return t_err; }
 
-int hsa_version(void) { return 100; }
+int hsa_version(void) { return 200; }
+
+hsa_status_t hsa_check_pointer(const void *p) {
+    if (!p) return fail(HSA_ERR_INVALID_ARG, "null pointer");
+    hsa_status_t st = check_pointer(p, "pointer");
+    return st == HSA_OK ? ok() : st;
+}
 
 hsa_status_t hsa_check(hsa_stream_t stream) {
     cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
@@ -199,6 +249,9 @@ hsa_status_t hsa_compress(const void *k, const void *v, hsa_dtype_t dt, int B, i
     DevInfo di;
     hsa_status_t st = device_info(di);
     if (st != HSA_OK) return st;
+    if ((st = check_pointers({{k, "k"}, {v, "v"}, {tok_begin, "tok_begin"}, {tok_end, "tok_end"}, {w, "w"},
+                              {kc, "kc"}, {vc, "vc"}})) != HSA_OK)
+        return st;
     if ((st = pending_error()) != HSA_OK) return st;
     hsa::CompressArgs a{k, v, B, d, in_sb, in_st, N_cap, tok_begin, tok_end, max_blocks, w, m, kc, vc, out_sb, out_se, E_cap};
     return launched(hsa::launch_compress(a, dt == HSA_BF16, di.num_sms, reinterpret_cast<cudaStream_t>(stream)),
@@ -223,6 +276,9 @@ hsa_status_t hsa_compress_learned(const void *k, const void *v, hsa_dtype_t dt, 
     DevInfo di;
     hsa_status_t st = device_info(di);
     if (st != HSA_OK) return st;
+    if ((st = check_pointers({{k, "k"}, {v, "v"}, {tok_begin, "tok_begin"}, {tok_end, "tok_end"}, {u, "u"},
+                              {bias, "bias"}, {kc, "kc"}, {vc, "vc"}})) != HSA_OK)
+        return st;
     if ((st = pending_error()) != HSA_OK) return st;
     hsa::CompressLearnedArgs a{k, v, B, d, in_sb, in_st, N_cap, tok_begin, tok_end, max_blocks, u, bias, m, L,
                                kc, vc, out_sb, out_se, E_cap};
@@ -251,6 +307,9 @@ hsa_status_t hsa_compress_append(const void *k_new, const void *v_new, hsa_dtype
     DevInfo di;
     hsa_status_t st = device_info(di);
     if (st != HSA_OK) return st;
+    if ((st = check_pointers({{k_new, "k_new"}, {v_new, "v_new"}, {pos0, "pos0"}, {w, "w"}, {state_k, "state_k"},
+                              {state_v, "state_v"}, {kc, "kc"}, {vc, "vc"}})) != HSA_OK)
+        return st;
     if ((st = pending_error()) != HSA_OK) return st;
     hsa::CompressAppendArgs a{k_new, v_new, B, T, d, new_sb, new_st, pos0, w, m, state_k, state_v, state_sb,
                               kc, vc, out_sb, out_se, E_cap};
@@ -302,6 +361,8 @@ hsa_status_t hsa_index_topk_workspace_size(int B, int T, int DI, int64_t E_cap, 
     if (B < 0 || T < 0 || E_cap < 0 || topk <= 0 || DI <= 0) return fail(HSA_ERR_INVALID_ARG, "bad size");
     if (DI != 16 && DI != 32 && DI != 64 && DI != 128)
         return fail(HSA_ERR_UNSUPPORTED, "indexer dim must be 16, 32, 64 or 128, got %d", DI);
+    if (B * (int64_t)T > kMaxRows) return fail(HSA_ERR_UNSUPPORTED, "B*T above 2^24");
+    if (E_cap > (int64_t)1 << 30) return fail(HSA_ERR_UNSUPPORTED, "E_cap above 2^30");
     DevInfo di;
     hsa_status_t st = device_info(di);
     if (st != HSA_OK) return st;
@@ -321,6 +382,7 @@ hsa_status_t hsa_index_topk(const int8_t *q_idx, int64_t q_sb, int64_t q_st, con
     if (topk <= 0 || topk > 4096) return fail(HSA_ERR_UNSUPPORTED, "topk must be in [1, 4096], got %d", topk);
     if (DI != 16 && DI != 32 && DI != 64 && DI != 128)
         return fail(HSA_ERR_UNSUPPORTED, "indexer dim must be 16, 32, 64 or 128, got %d", DI);
+    if (B * (int64_t)T > kMaxRows) return fail(HSA_ERR_UNSUPPORTED, "B*T above 2^24");
     const int rows = B * T;
     if (rows == 0) return ok();
     if (!q_idx || !k_idx || !q_pos0 || !idx_out || !cnt_out) return fail(HSA_ERR_INVALID_ARG, "null pointer");
@@ -331,6 +393,9 @@ hsa_status_t hsa_index_topk(const int8_t *q_idx, int64_t q_sb, int64_t q_st, con
     DevInfo di;
     hsa_status_t st = device_info(di);
     if (st != HSA_OK) return st;
+    if ((st = check_pointers({{q_idx, "q_idx"}, {k_idx, "k_idx"}, {q_pos0, "q_pos0"}, {idx_out, "idx_out"},
+                              {cnt_out, "cnt_out"}})) != HSA_OK)
+        return st;
     hsa::IndexArgs a{q_idx, q_sb, q_st, k_idx, k_sb, k_se, E_cap, B, T, DI, q_pos0, m, topk, idx_out, cnt_out};
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (E_cap == 0) {
@@ -344,6 +409,7 @@ hsa_status_t hsa_index_topk(const int8_t *q_idx, int64_t q_sb, int64_t q_st, con
     if (!ws || ws_bytes < ch.bytes)
         return fail(HSA_ERR_WORKSPACE, "index workspace needs %zu bytes, got %zu", ch.bytes, ws_bytes);
     if ((reinterpret_cast<uintptr_t>(ws) & 255) != 0) return fail(HSA_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+    if ((st = check_pointer(ws, "workspace")) != HSA_OK) return st;
     if ((st = pending_error()) != HSA_OK) return st;
     if (ch.fused) return launched(hsa::launch_index_fused(a, ch.fp, ws, s), "index_topk (fused)");
     if (ch.prefill) return launched(hsa::launch_index_prefill(a, ch.pp, ws, di.num_sms, s), "index_topk (tensor cores)");
@@ -384,6 +450,8 @@ hsa_status_t hsa_attn_decode(const void *q, hsa_dtype_t dt, int B, int H, int d,
         return fail(HSA_ERR_WORKSPACE, "decode workspace needs %zu bytes, got %zu", p.total, ws_bytes);
     if (p.total > 0 && (reinterpret_cast<uintptr_t>(ws) & 255) != 0)
         return fail(HSA_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+    if ((st = check_pointers({{cnt, "cnt"}, {lse, "lse"}, {p.total > 0 ? ws : nullptr, "workspace"}})) != HSA_OK)
+        return st;
     if ((st = pending_error()) != HSA_OK) return st;
     hsa::AttnArgs a{};
     a.q = q; a.rows = B; a.T = 1; a.H = H; a.d = d;
@@ -425,7 +493,7 @@ hsa_status_t hsa_attn_prefill(const void *q, hsa_dtype_t dt, int B, int T, int H
     if (B == 0 || T == 0) return ok();
     DevInfo di;
     if ((st = device_info(di)) != HSA_OK) return st;
-    if ((int64_t)B * T > (1ll << 24)) return fail(HSA_ERR_UNSUPPORTED, "B*T above 2^24");
+    if ((st = check_pointers({{cnt, "cnt"}, {lse, "lse"}})) != HSA_OK) return st;
     if ((st = pending_error()) != HSA_OK) return st;
     const bool dense = idx == nullptr;
     hsa::AttnArgs a{};
@@ -484,6 +552,7 @@ extern "C" hsa_status_t hsa_index_topk_noalloc(const int8_t *q_idx, int64_t q_sb
     if (topk <= 0 || topk > 4096) return fail(HSA_ERR_UNSUPPORTED, "topk must be in [1, 4096], got %d", topk);
     if (DI != 16 && DI != 32 && DI != 64 && DI != 128)
         return fail(HSA_ERR_UNSUPPORTED, "indexer dim must be 16, 32, 64 or 128, got %d", DI);
+    if (B * (int64_t)T > kMaxRows) return fail(HSA_ERR_UNSUPPORTED, "B*T above 2^24");
     const int rows = B * T;
     if (rows == 0) return ok();
     if (!q_idx || !k_idx || !q_pos0 || !idx_out || !cnt_out) return fail(HSA_ERR_INVALID_ARG, "null pointer");
@@ -494,6 +563,9 @@ extern "C" hsa_status_t hsa_index_topk_noalloc(const int8_t *q_idx, int64_t q_sb
     DevInfo di;
     hsa_status_t st = device_info(di);
     if (st != HSA_OK) return st;
+    if ((st = check_pointers({{q_idx, "q_idx"}, {k_idx, "k_idx"}, {q_pos0, "q_pos0"}, {idx_out, "idx_out"},
+                              {cnt_out, "cnt_out"}})) != HSA_OK)
+        return st;
     hsa::IndexArgs a{q_idx, q_sb, q_st, k_idx, k_sb, k_se, E_cap, B, T, DI, q_pos0, m, topk, idx_out, cnt_out};
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (E_cap == 0) {
@@ -541,6 +613,9 @@ hsa_status_t hsa_index_scores(const int8_t *q_idx, int64_t q_sb, int64_t q_st, c
     hsa_status_t st = device_info(di);
     if (st != HSA_OK) return st;
     if ((st = pending_error()) != HSA_OK) return st;
+    if ((st = check_pointers({{q_idx, "q_idx"}, {k_idx, "k_idx"}, {idx, "idx"}, {cnt, "cnt"}, {scores, "scores"}})) !=
+        HSA_OK)
+        return st;
     hsa::IndexScoreArgs a{q_idx, q_sb, q_st, k_idx, k_sb, k_se, E_cap, B, T, DI, idx, cnt, topk, scores};
     return launched(hsa::launch_index_scores(a, reinterpret_cast<cudaStream_t>(stream)), "index_scores");
 }
@@ -555,6 +630,8 @@ hsa_status_t hsa_topk_merge(const int32_t *scores, const int32_t *idx, int rows,
     hsa_status_t st = device_info(di);
     if (st != HSA_OK) return st;
     if ((st = pending_error()) != HSA_OK) return st;
+    if ((st = check_pointers({{scores, "scores"}, {idx, "idx"}, {idx_out, "idx_out"}, {cnt_out, "cnt_out"}})) != HSA_OK)
+        return st;
     hsa::TopkMergeArgs a{scores, idx, rows, n, topk, idx_out, cnt_out};
     return launched(hsa::launch_topk_merge(a, reinterpret_cast<cudaStream_t>(stream)), "topk_merge");
 }
@@ -572,6 +649,9 @@ hsa_status_t hsa_lse_merge(const void *parts_o, const float *parts_lse, hsa_dtyp
     hsa_status_t st = device_info(di);
     if (st != HSA_OK) return st;
     if ((st = pending_error()) != HSA_OK) return st;
+    if ((st = check_pointers({{parts_o, "parts_o"}, {parts_lse, "parts_lse"}, {out, "out"}, {lse_out, "lse_out"}})) !=
+        HSA_OK)
+        return st;
     hsa::LseMergeArgs a{parts_o, parts_lse, S, rows, H, d, out, lse_out};
     return launched(hsa::launch_lse_merge(a, dt == HSA_BF16, reinterpret_cast<cudaStream_t>(stream)), "lse_merge");
 }
@@ -594,6 +674,9 @@ hsa_status_t hsa_rmsnorm_rope(void *x, hsa_dtype_t dt, int B, int H, int d, int6
     hsa_status_t st = device_info(di);
     if (st != HSA_OK) return st;
     if ((st = pending_error()) != HSA_OK) return st;
+    if ((st = check_pointers({{x, "x"}, {n_begin, "n_begin"}, {n_end, "n_end"}, {pos_base, "pos_base"},
+                              {gamma, "gamma"}})) != HSA_OK)
+        return st;
     hsa::NormRopeArgs a{x, B, H, d, x_sb, x_sn, n_cap, n_begin, n_end, max_rows, pos_base, pos_stride, pos_offset,
                         gamma, eps, rope_dims, {}};
     for (int k = 0; k < rope_dims / 2; ++k) a.inv_freq[k] = pow((double)theta, -2.0 * k / rope_dims);
@@ -617,6 +700,7 @@ hsa_status_t hsa_attn_finalize(void *out, float *lse, hsa_dtype_t dt, int B, int
     hsa_status_t st = device_info(di);
     if (st != HSA_OK) return st;
     if ((st = pending_error()) != HSA_OK) return st;
+    if ((st = check_pointers({{out, "out"}, {lse, "lse"}, {q_pos0, "q_pos0"}, {sink, "sink"}})) != HSA_OK) return st;
     hsa::FinalizeArgs a{out, lse, B, T, H, d, q_pos0, sink, rope_dims, {}};
     for (int k = 0; k < rope_dims / 2; ++k) a.inv_freq[k] = pow((double)theta, -2.0 * k / rope_dims);
     return launched(hsa::launch_attn_finalize(a, dt == HSA_BF16, reinterpret_cast<cudaStream_t>(stream)),

@@ -18,7 +18,10 @@
  *
  * Conventions (all entry points):
  *   - Every buffer argument is caller-owned DEVICE memory of the current CUDA
- *     device unless stated otherwise.  The library never allocates, frees or
+ *     device (or managed memory) unless stated otherwise.  Each call classifies
+ *     its pointers with cudaPointerGetAttributes before it enqueues anything and
+ *     refuses host memory (pageable or pinned) and other devices' memory with
+ *     HSA_ERR_INVALID_ARG.  The library never allocates, frees or
  *     synchronises (except hsa_check); all work is enqueued on `stream`
  *     (a cudaStream_t; NULL is the legacy default stream).
  *   - Strides are in ELEMENTS.  The innermost (channel) dimension is
@@ -84,6 +87,13 @@ HSA_API int hsa_version(void);
 /* Synchronises `stream`, then reports (and clears) any pending asynchronous
  * CUDA error and the device range-violation flag of the current device. */
 HSA_API hsa_status_t hsa_check(hsa_stream_t stream);
+
+/* The pointer classification every entry point applies to its buffers (no
+ * counterpart in the pages: a guard of this library's boundary).  HSA_OK if
+ * `p` is device memory of the current device or managed memory;
+ * HSA_ERR_INVALID_ARG (with the reason in hsa_last_error) for NULL, host memory
+ * (pageable or pinned) and another device's memory.  Enqueues nothing. */
+HSA_API hsa_status_t hsa_check_pointer(const void *p);
 
 /*
  * hsa_compress -- KV compression (QbitAI article, 混合注意力机制: CSA step 1
@@ -177,7 +187,7 @@ HSA_API hsa_status_t hsa_compress_append(const void *k_new, const void *v_new, h
  *   ws         workspace of hsa_index_topk_workspace_size bytes
  * DI a multiple of 16 in [16, 128]; 1 <= topk <= 4096; m >= 1.
  * Results are bit-identical for every input (ties included) and independent
- * of B, T and the launch configuration.
+ * of B, T and the launch configuration.  B * T <= 2^24.
  */
 HSA_API hsa_status_t hsa_index_topk_workspace_size(int B, int T, int DI, int64_t E_cap, int topk,
                                            size_t *bytes);
@@ -249,8 +259,8 @@ HSA_API hsa_status_t hsa_index_topk_noalloc(const int8_t *q_idx, int64_t q_sb, i
  *              128 slots, one thread-block cluster per (sequence, 64 heads), and
  *              the workspace holds their fp32 partials, about B * H/64 *
  *              ceil((topk + window) / 128) * 33,280 bytes.
- * Every pointer is a device pointer (memory the GPU can address); host memory,
- * pinned or not, is not accepted.
+ * Every pointer is a device pointer; host memory, pinned or not, is refused
+ * with HSA_ERR_INVALID_ARG before anything is enqueued.
  * bf16: d in {64, 128}, H a multiple of 16 up to 128.  fp32: d a multiple of
  * 32 up to 256, any H.
  */

@@ -76,3 +76,11 @@ def test_python_binding_refuses_to_run_without_the_library(tmp_path, monkeypatch
     with pytest.raises(ImportError):
         L._load()
     importlib.reload(L)
+
+
+def test_pointer_classifier_refuses_without_a_device(lib):
+    # no GPU here: nothing can be classified as device memory
+    import numpy as np
+    a = np.zeros(16, dtype=np.uint8)
+    assert lib.lib.hsa_check_pointer(a.ctypes.data) == lib.HSA_ERR_INVALID_ARG
+    assert lib.lib.hsa_check_pointer(None) == lib.HSA_ERR_INVALID_ARG

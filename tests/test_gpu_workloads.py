@@ -1,10 +1,12 @@
 """Parity of the whole hot path (compress -> index/top-k -> attention) on the
 five workloads at their full sizes, in the launch configuration bench.py uses.
 
-Decode workloads are checked on every sequence; the 8192-token prefill on a
-seeded sample of query rows (first 32, last 32 and every 256th), which the
-oracle computes one by one.  Top-k indices and counts must match bit-exactly,
-outputs within the bf16 tolerance (max 2e-2, mean 2e-3) of the fp64 oracle."""
+Decode workloads are checked on every sequence.  On the 8192-token chunked
+prefill every query row's top-k indices and count are checked; outputs and
+log-sum-exps on every 16th row plus the first and last 64 rows (644 rows), which
+the oracle computes one by one.  Top-k indices and counts must match
+bit-exactly, outputs within the bf16 tolerance (max 2e-2, mean 2e-3) of the
+fp64 oracle."""
 import numpy as np
 import pytest
 import torch
@@ -81,7 +83,8 @@ def test_decode_workload(lib, name):
 
 
 def _sample_rows(T):
-    rows = set(range(min(32, T))) | set(range(max(0, T - 32), T)) | set(range(0, T, 256))
+    """Rows whose outputs are compared on long chunks: every 16th, the first 64 and the last 64."""
+    rows = set(range(min(64, T))) | set(range(max(0, T - 64), T)) | set(range(0, T, 16))
     return np.array(sorted(rows), dtype=np.int64)
 
 
@@ -108,15 +111,21 @@ def test_prefill_workload(lib, name):
     lib.hsa_attn_prefill(x.q.to(dev), kc, vc, m, idx, cnt, kr, vr, wl.window, pos0, wl.scale, out, lse, wsa)
     lib.hsa_check()
 
+    assert B == 1
     rows = _sample_rows(T) if T > 4096 else np.arange(T, dtype=np.int64)
     rows_b = np.zeros(len(rows), np.int64)
     rows_p = int(x.q_pos0[0]) + rows
     oidx = None
     if wl.kind == "csa":
-        qi = x.q_idx.numpy().reshape(B * T, wl.DI)[rows]
-        oidx, ocnt = oracle.index_topk_rows(qi, rows_b, rows_p, x.k_idx.numpy(), m, wl.topk)
-        assert np.array_equal(cnt.view(B * T).cpu().numpy()[rows], ocnt)
-        assert np.array_equal(idx.view(B * T, wl.topk).cpu().numpy()[rows], oidx)
+        # every query row's selection, bit-exact
+        all_rows = np.arange(T, dtype=np.int64)
+        aidx, acnt = oracle.index_topk_rows(x.q_idx.numpy().reshape(B * T, wl.DI), np.zeros(T, np.int64),
+                                            int(x.q_pos0[0]) + all_rows, x.k_idx.numpy(), m, wl.topk)
+        gcnt = cnt.view(B * T).cpu().numpy()
+        gidx = idx.view(B * T, wl.topk).cpu().numpy()
+        bad = np.flatnonzero((gcnt != acnt) | (gidx != aidx).any(axis=1))
+        assert bad.size == 0, f"{bad.size} of {T} rows differ from the oracle's top-k, first {bad[:8].tolist()}"
+        oidx = aidx[rows]
     okc, ovc = _oracle_cache(x, E, x.ctx_len.numpy())
     qr = bf16_bits(x.q.reshape(B * T, H, d))[rows]
     ro, rl = oracle.attn_rows(qr, rows_b, rows_p, okc, ovc, m, oidx, bf16_bits(x.k_raw), bf16_bits(x.v_raw),
