@@ -1,29 +1,42 @@
 #!/usr/bin/env python3
-"""Benchmark of the hybrid compressed/sparse attention hot path on one B300.
+"""Benchmark of the hybrid compressed/sparse attention hot path on B300.
 
-A step is one decode step of one CSA attention layer over a batch of 4
-sequences at 1,048,576 cached tokens (V4-Pro shape: 128 query heads, head dim
+The headline step is one decode step of one CSA attention layer over a batch of
+4 sequences at 1,048,576 cached tokens (V4-Pro shape: 128 query heads, head dim
 128, m = 4 -> 262,144 compressed entries, int8 indexer dim 64, top-k 1024,
 128-token window):
-  1. hsa_compress   -- fold the block completed by the new token into its entry
-  2. hsa_index_topk -- int8 scores of all 262,144 entries, exact top-1024
-  3. hsa_attn_decode -- split-KV attention over the 1024 entries + 128 raw tokens,
-                        log-sum-exp merge of the splits.
-Inputs are seeded synthetic tensors; the timed steps rotate over R replicas of
-the per-step inputs whose indexer keys alone exceed 4x the L2 cache, so every
-step reads them from HBM.  One CUDA graph holds a block of steps; the timed
-region is exactly K steps.
+  1. hsa_compress    -- fold the block completed by the new token into its entry
+  2. hsa_index_topk  -- int8 scores of all 262,144 entries, exact top-1024
+  3. hsa_attn_decode -- attention over the 1024 entries + 128 raw tokens, split
+                        over 128-item tiles and merged by log-sum-exp.
+The same timing runs two more decode rows: the V4-Flash-shaped CSA step (B = 8
+at 131,072 tokens, 64 heads, top-k 512) and the HCA step (B = 16, lengths
+uniform in [262144, 1048576], m = 128, dense over all entries + window).
+
+Inputs are seeded synthetic tensors.  Every per-step buffer (query, indexer
+keys, raw and compressed caches, outputs) exists in R replicas that the steps
+rotate over, and the replicas' bytes exceed 4x the L2 cache, so a step reads its
+inputs from HBM.  CUDA graphs hold the steps; the timed region is exactly K
+steps (barrier + synchronize on both sides, max over ranks), followed by at
+least 20 further replays of the same K steps whose median is reported beside it.
+The chunked-prefill rows (8192 new tokens on a 1M-token cache, one HCA and one
+CSA layer) time each call alone after an L2 flush.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl {hsa,reference}]
-Prints one JSON line on rank 0.
+Prints one JSON line on rank 0.  With --gpus N > 1 and no launcher environment,
+the script starts N ranks itself (one process per GPU, NCCL), each running the
+same replicas on its own GPU (weak scaling, no data-path collective).
 """
 from __future__ import annotations
 
 import argparse
+import ctypes
+import hashlib
 import json
 import math
 import os
 import platform
+import socket
 import statistics
 import subprocess
 import sys
@@ -36,103 +49,170 @@ import torch
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-from compressed_attention_compress_b300.inputs import WORKLOADS, block_weights  # noqa: E402
+from compressed_attention_compress_b300.inputs import WORKLOADS, block_weights, context_lengths, T_LEN  # noqa: E402
 
-WL = WORKLOADS["pro_csa_decode"]
+HEADLINE = "pro_csa_decode"
+EXTRA_DECODE = ("flash_csa_decode", "hca_decode")
+METRIC = "decode queries/s at 1M ctx (V4-Pro-shaped CSA layer, B=4)"
+UNIT = "queries/s"
 
-# DRAM bytes (read + write) of one index_fused_kernel launch on this workload, from the
-# ncu capture summarised in profiles/index_fused_kernel_pro_csa_1M_B4.md; reported only
-# while the kernel's sources are the ones that capture ran.
-INDEX_TRAFFIC = {
-    "bytes": 67258368 + 110336,
-    "sources": {
-        "compressed_attention_compress_b300/csrc/index_fused.cu":
-            "fd9e0083f6ed2eebb211bcb3ff11a3142598ba316ffa91176b925dcc9d2cf824",
-        "compressed_attention_compress_b300/csrc/common.cuh":
-            "1c50e4616466d69022320548d2a47c9c9d2aef65c6b5dca650519a168e3275b2",
-        "compressed_attention_compress_b300/csrc/block_scan.cuh":
-            "ac0c74255584e15eaea3aa69860c5b08cd4267e432e4e9db82d6c3de8245161a",
+# DRAM bytes (read + write) of one launch of a kernel on a workload, from an ncu
+# capture of that kernel; reported only while the kernel's sources are the ones
+# that capture ran (sha256 of each file).
+TRAFFIC = {
+    ("index_fused_kernel", "pro_csa_decode"): {
+        "bytes": 67258368 + 110336,
+        "sources": {
+            "compressed_attention_compress_b300/csrc/index_fused.cu":
+                "fd9e0083f6ed2eebb211bcb3ff11a3142598ba316ffa91176b925dcc9d2cf824",
+            "compressed_attention_compress_b300/csrc/common.cuh":
+                "1c50e4616466d69022320548d2a47c9c9d2aef65c6b5dca650519a168e3275b2",
+            "compressed_attention_compress_b300/csrc/block_scan.cuh":
+                "ac0c74255584e15eaea3aa69860c5b08cd4267e432e4e9db82d6c3de8245161a",
+        },
     },
 }
 
 
-def index_traffic():
-    import hashlib
-    for rel, want in INDEX_TRAFFIC["sources"].items():
+def measured_traffic(kernel: str, workload: str):
+    t = TRAFFIC.get((kernel, workload))
+    if t is None:
+        return None
+    for rel, want in t["sources"].items():
         with open(os.path.join(ROOT, rel), "rb") as f:
             if hashlib.sha256(f.read()).hexdigest() != want:
                 return None
-    return INDEX_TRAFFIC["bytes"]
-METRIC = "decode queries/s at 1M ctx (V4-Pro-shaped CSA layer, B=4)"
-UNIT = "queries/s"
+    return t["bytes"]
 
 
 # ----------------------------------------------------------------- helpers
 
-def algorithmic_bytes(wl, cnt_total: int):
-    """Bytes the method must move in one decode step (raw cache outside the window not counted)."""
-    B, E, DI, d = wl.B, wl.N // wl.m, wl.DI, wl.d
-    idx_bytes = B * E * DI + B * DI + 2 * B * wl.topk * 4 + 2 * B * 4      # keys, queries, idx/cnt write+read
-    gather = cnt_total * 2 * d * 2                                          # selected K and V entries
-    window = B * min(wl.window, wl.N) * 2 * d * 2
+def algorithmic_bytes(wl, ctx, cnt_total: int):
+    """Bytes the method must move in one decode step (raw cache outside the window
+    not counted): indexer keys and query, the top-k written and read back, the
+    selected (CSA) or all visible (HCA) compressed K and V rows, the window's raw K
+    and V rows, q and out, and the new block's compression."""
+    B, d, m = wl.B, wl.d, wl.m
+    E = [int(c) // m for c in ctx]
+    win = sum(min(wl.window, int(c)) for c in ctx)
+    if wl.kind == "csa":
+        index = sum(E) * wl.DI + B * wl.DI + 2 * B * wl.topk * 4 + 2 * B * 4
+        entries = cnt_total * 2 * d * 2
+    else:
+        index = 0
+        entries = sum(E) * 2 * d * 2
+    window = win * 2 * d * 2
     qo = 2 * B * wl.H * d * 2
-    compress = B * wl.m * 2 * d * 2 + B * 2 * d * 2
-    return {"index_topk": idx_bytes, "step": idx_bytes + gather + window + qo + compress}
+    compress = B * m * 2 * d * 2 + B * 2 * d * 2
+    attn = entries + window + qo + (2 * B * wl.topk * 4 if wl.kind == "csa" else 0)
+    return {"index_topk": index, "attn_decode": attn, "compress": compress,
+            "step": index + entries + window + qo + compress}
+
+
+def pci_bus_id(dev_index: int):
+    """PCI bus id of CUDA device `dev_index` in NVML's form, so that NVML and
+    nvidia-smi read the same GPU whatever CUDA_VISIBLE_DEVICES maps; None if unknown."""
+    try:
+        p = torch.cuda.get_device_properties(dev_index)
+        return f"{p.pci_domain_id:08X}:{p.pci_bus_id:02X}:{p.pci_device_id:02X}.0"
+    except Exception:  # noqa: BLE001
+        return None
+
+
+class _CtypesNvml:
+    """Read-only NVML through libnvidia-ml (clock and clock-event reasons), for
+    when the pynvml module is not importable."""
+
+    def __init__(self, bus_id):
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit_v2 failed")
+        self.h = ctypes.c_void_p()
+        if self.lib.nvmlDeviceGetHandleByPciBusId_v2(bus_id.encode(), ctypes.byref(self.h)) != 0:
+            raise RuntimeError(f"nvmlDeviceGetHandleByPciBusId_v2({bus_id}) failed")
+        fn = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None)
+        self._reasons_fn = fn if fn is not None else self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+
+    def sm_clock(self):
+        c = ctypes.c_uint()
+        self.lib.nvmlDeviceGetClockInfo(self.h, ctypes.c_int(1), ctypes.byref(c))  # NVML_CLOCK_SM
+        return c.value
+
+    def max_sm_clock(self):
+        c = ctypes.c_uint()
+        self.lib.nvmlDeviceGetMaxClockInfo(self.h, ctypes.c_int(1), ctypes.byref(c))
+        return c.value
+
+    def reasons(self):
+        r = ctypes.c_ulonglong()
+        self._reasons_fn(self.h, ctypes.byref(r))
+        return r.value
 
 
 class ClockSampler:
-    """Samples the SM clock and throttle reasons during the timed region: NVML
-    (what nvidia-smi reads) polled from a thread, else an `nvidia-smi -lms` child."""
+    """Samples the SM clock and clock-event (throttle) reasons while the timed work
+    runs: NVML (pynvml, else libnvidia-ml through ctypes) polled from a thread,
+    else an `nvidia-smi -lms` child.  Only reads; changes no setting."""
 
     _NAMES = {0x8: "hw_slowdown", 0x40: "hw_thermal_slowdown", 0x20: "sw_thermal_slowdown", 0x4: "sw_power_cap",
               0x80: "hw_power_brake_slowdown"}
 
-    def __init__(self, dev_index: int, period_s: float = 0.005):
+    def __init__(self, dev_index: int, period_s: float = 0.01):
         self.samples, self.reasons, self.max_mhz = [], set(), None
         self.period, self._stop = period_s, threading.Event()
         self.mode, self.err = None, None
+        self.bus_id = pci_bus_id(dev_index)
+        self.dev_index = dev_index
         try:
             import pynvml
             pynvml.nvmlInit()
-            self.nvml = pynvml
-            self.h = pynvml.nvmlDeviceGetHandleByIndex(dev_index)
-            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
+            h = pynvml.nvmlDeviceGetHandleByPciBusId(self.bus_id)
+            self._clock = lambda: pynvml.nvmlDeviceGetClockInfo(h, pynvml.NVML_CLOCK_SM)
+            self._reasons = lambda: pynvml.nvmlDeviceGetCurrentClocksEventReasons(h)
+            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(h, pynvml.NVML_CLOCK_SM)
             self.mode = "nvml"
         except Exception as e:  # noqa: BLE001
-            self.err = f"nvml: {e}"
-            self.mode = "smi"
-        self.dev_index = dev_index
+            self.err = f"pynvml: {e}"
+            try:
+                n = _CtypesNvml(self.bus_id)
+                self._clock, self._reasons = n.sm_clock, n.reasons
+                self.max_mhz = n.max_sm_clock()
+                self.mode = "nvml-ctypes"
+            except Exception as e2:  # noqa: BLE001
+                self.err += f"; libnvidia-ml: {e2}"
+                self.mode = "smi"
 
     def _run(self):
         while not self._stop.is_set():
             try:
-                self.samples.append(self.nvml.nvmlDeviceGetClockInfo(self.h, self.nvml.NVML_CLOCK_SM))
-                r = self.nvml.nvmlDeviceGetCurrentClocksEventReasons(self.h)
+                self.samples.append(self._clock())
+                r = self._reasons()
                 for bit, name in self._NAMES.items():
                     if r & bit:
                         self.reasons.add(name)
             except Exception as e:  # noqa: BLE001
-                self.err = f"nvml poll: {e}"
+                self.err = f"poll: {e}"
             time.sleep(self.period)
 
     def __enter__(self):
-        if self.mode == "nvml":
+        if self.mode != "smi":
             self.t = threading.Thread(target=self._run, daemon=True)
             self.t.start()
         else:
             q = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
                  "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
             try:
-                self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.dev_index), f"--query-gpu={q}",
+                self.proc = subprocess.Popen(["nvidia-smi", "-i", self.bus_id or str(self.dev_index), f"--query-gpu={q}",
                                               "--format=csv,noheader,nounits", "-lms", "50"],
                                              stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                time.sleep(0.5)  # the child's first sample
             except Exception as e:  # noqa: BLE001
                 self.proc = None
                 self.err = (self.err or "") + f"; smi: {e}"
         return self
 
     def __exit__(self, *a):
-        if self.mode == "nvml":
+        if self.mode != "smi":
             self._stop.set()
             self.t.join()
         elif getattr(self, "proc", None) is not None:
@@ -154,8 +234,9 @@ class ClockSampler:
 
     def summary(self):
         d = {"sm_mhz": statistics.median(self.samples) if self.samples else None, "sm_max_mhz": self.max_mhz,
-             "reasons": sorted(self.reasons), "samples": len(self.samples), "source": self.mode}
-        if self.err:
+             "reasons": sorted(self.reasons), "samples": len(self.samples), "source": self.mode,
+             "window": "warm-up, the timed K steps and the repeated replays"}
+        if self.err and not self.samples:
             d["note"] = self.err
         return d
 
@@ -175,7 +256,7 @@ def load_peaks(kind: str = "hbm_gbs"):
 
 # ------------------------------------------------------------ distributed
 
-def dist_setup(args):
+def dist_setup():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
@@ -198,21 +279,39 @@ def max_over_ranks(x: float, ws: int) -> float:
     if ws <= 1:
         return x
     import torch.distributed as dist
-    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    dev = "cuda" if torch.cuda.is_available() and dist.get_backend() == "nccl" else "cpu"
     t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
 
 
-# ------------------------------------------------------------- hsa arm
+def _free_port() -> int:
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_entry(local_rank: int, argv, n: int, port: int):
+    os.environ.update({"RANK": str(local_rank), "LOCAL_RANK": str(local_rank), "WORLD_SIZE": str(n),
+                       "LOCAL_WORLD_SIZE": str(n), "MASTER_ADDR": "127.0.0.1", "MASTER_PORT": str(port)})
+    main(argv)
+
+
+def spawn_ranks(argv, n: int):
+    """Start n ranks of this script (one process per GPU) when no launcher did."""
+    import torch.multiprocessing as mp
+    mp.start_processes(_rank_entry, args=(argv, n, _free_port()), nprocs=n, start_method="spawn", join=True)
+
+
+# ------------------------------------------------------------- decode rows
 
 class DecodeBench:
-    """Device buffers and the three C-ABI calls of one decode step."""
+    """Device buffers of R input replicas and the C-ABI calls of one decode step."""
 
     def __init__(self, wl, replicas: int, seed_base: int, dev):
         from compressed_attention_compress_b300 import _lib as L
         self.L, self.wl, self.dev, self.R = L, wl, dev, replicas
-        B, N, H, d, m, DI = wl.B, wl.N, wl.H, wl.d, wl.m, wl.DI
+        B, N, H, d, m = wl.B, wl.N, wl.H, wl.d, wl.m
         E = N // m
         g = torch.Generator(device=dev)
         g.manual_seed(seed_base)
@@ -229,58 +328,88 @@ class DecodeBench:
         def randint8(shape):
             return torch.randint(-127, 128, shape, generator=g, device=dev, dtype=torch.int16).to(torch.int8)
 
-        self.k_raw = randn_bf16((B, N, d))
-        self.v_raw = randn_bf16((B, N, d))
+        if wl.len_hi:
+            ctx = context_lengths(B, wl.len_lo, wl.len_hi, 1000 * wl.wid + T_LEN)
+        else:
+            ctx = torch.full((B,), N, dtype=torch.int64)
+        self.ctx_host = ctx
+        self.ctx = ctx.to(dev)
+        self.pos0 = self.ctx - 1
+        # the block the newest complete block boundary closes, one per sequence
+        last = torch.div(self.ctx, m, rounding_mode="floor") * m
+        self.tb, self.te = (last - m).clamp(min=0), last
         self.w = block_weights(m, seed_base + 6).to(dev)
-        self.kc = torch.empty((B, E, d), dtype=torch.bfloat16, device=dev)
-        self.vc = torch.empty_like(self.kc)
         zeros = torch.zeros(B, dtype=torch.int64, device=dev)
-        full = torch.full((B,), N, dtype=torch.int64, device=dev)
-        L.hsa_compress(self.k_raw, self.v_raw, zeros, full, E, self.w, m, self.kc, self.vc)  # build the cache
-        self.ctx = full
-        self.pos0 = full - 1
-        self.tb = full - m                # the block completed by the new token
-        self.te = full
-        self.q = [randn_bf16((B, H, d)) for _ in range(replicas)]
-        self.qi = [randint8((B, 1, DI)) for _ in range(replicas)]
-        self.ki = [randint8((B, E, DI)) for _ in range(replicas)]
-        self.idx = [torch.empty((B, 1, wl.topk), dtype=torch.int32, device=dev) for _ in range(replicas)]
-        self.cnt = [torch.empty((B, 1), dtype=torch.int32, device=dev) for _ in range(replicas)]
-        self.out = [torch.empty((B, H, d), dtype=torch.bfloat16, device=dev) for _ in range(replicas)]
-        self.lse = [torch.empty((B, H), dtype=torch.float32, device=dev) for _ in range(replicas)]
-        self.ws_i = L.workspace(L.hsa_index_topk_workspace_size(B, 1, DI, E, wl.topk), device=dev)
-        self.ws_a = L.workspace(L.hsa_attn_decode_workspace_size(torch.bfloat16, B, H, d, E, m, wl.topk, wl.window),
+        self.k_raw, self.v_raw, self.kc, self.vc, self.q = [], [], [], [], []
+        self.qi, self.ki, self.idx, self.cnt, self.out, self.lse = [], [], [], [], [], []
+        for r in range(replicas):
+            kr, vr = randn_bf16((B, N, d)), randn_bf16((B, N, d))
+            kc = torch.empty((B, E, d), dtype=torch.bfloat16, device=dev)
+            vc = torch.empty_like(kc)
+            L.hsa_compress(kr, vr, zeros, self.ctx, E, self.w, m, kc, vc)  # the cache before the step
+            self.k_raw.append(kr)
+            self.v_raw.append(vr)
+            self.kc.append(kc)
+            self.vc.append(vc)
+            self.q.append(randn_bf16((B, H, d)))
+            self.out.append(torch.empty((B, H, d), dtype=torch.bfloat16, device=dev))
+            self.lse.append(torch.empty((B, H), dtype=torch.float32, device=dev))
+            if wl.kind == "csa":
+                self.qi.append(randint8((B, 1, wl.DI)))
+                self.ki.append(randint8((B, E, wl.DI)))
+                self.idx.append(torch.empty((B, 1, wl.topk), dtype=torch.int32, device=dev))
+                self.cnt.append(torch.empty((B, 1), dtype=torch.int32, device=dev))
+        self.ws_i = None
+        if wl.kind == "csa":
+            self.ws_i = L.workspace(L.hsa_index_topk_workspace_size(B, 1, wl.DI, E, wl.topk), device=dev)
+        self.ws_a = L.workspace(L.hsa_attn_decode_workspace_size(torch.bfloat16, B, H, d, E, m,
+                                                                 wl.topk if wl.kind == "csa" else 0, wl.window),
                                 device=dev)
         torch.cuda.synchronize(dev)
+        self.calls = ("compress", "index_topk", "attn_decode") if wl.kind == "csa" else ("compress", "attn_decode")
+
+    def replica_bytes(self) -> int:
+        per = sum(t.numel() * t.element_size() for t in (self.k_raw[0], self.v_raw[0], self.kc[0], self.vc[0]))
+        if self.wl.kind == "csa":
+            per += self.ki[0].numel()
+        return per
 
     def compress(self, r):
-        self.L.hsa_compress(self.k_raw, self.v_raw, self.tb, self.te, 1, self.w, self.wl.m, self.kc, self.vc)
+        self.L.hsa_compress(self.k_raw[r], self.v_raw[r], self.tb, self.te, 1, self.w, self.wl.m, self.kc[r],
+                            self.vc[r])
 
-    def index(self, r):
-        self.L.hsa_index_topk(self.qi[r], self.ki[r], self.pos0, self.wl.m, self.wl.topk, self.idx[r], self.cnt[r],
-                              self.ws_i)
+    def index(self, r, qi=None):
+        self.L.hsa_index_topk(self.qi[r] if qi is None else qi, self.ki[r], self.pos0, self.wl.m, self.wl.topk,
+                              self.idx[r], self.cnt[r], self.ws_i)
 
-    def attn(self, r):
+    def attn(self, r, q=None, kv_shared=False):
         wl = self.wl
-        self.L.hsa_attn_decode(self.q[r], self.kc, self.vc, wl.m, self.idx[r].view(wl.B, wl.topk),
-                               self.cnt[r].view(wl.B), self.k_raw, self.v_raw, wl.window, self.ctx, wl.scale,
-                               self.out[r], self.lse[r], self.ws_a)
+        csa = wl.kind == "csa"
+        vc = self.kc[r] if kv_shared else self.vc[r]
+        vr = self.k_raw[r] if kv_shared else self.v_raw[r]
+        self.L.hsa_attn_decode(self.q[r] if q is None else q, self.kc[r], vc, wl.m,
+                               self.idx[r].view(wl.B, wl.topk) if csa else None,
+                               self.cnt[r].view(wl.B) if csa else None, self.k_raw[r], vr, wl.window, self.ctx,
+                               wl.scale, self.out[r], self.lse[r], self.ws_a)
 
     def step(self, r):
         self.compress(r)
-        self.index(r)
+        if self.wl.kind == "csa":
+            self.index(r)
         self.attn(r)
 
+    def cnt_total(self) -> int:
+        if self.wl.kind != "csa":
+            return 0
+        return int(self.cnt[0].sum())
 
-KERNELS_PER_STEP = 3  # compress, fused indexer/top-k, cluster attention (split merge inside)
 
-
-def capture_block(bench, steps, start, events=None):
-    """One CUDA graph of `steps` consecutive steps (replica (start+i) % R).  The new
-    block's compression runs on a second stream, beside the indexer (which does not
-    read the compressed cache); attention waits for both.  With `events`
-    ([step][4] external CUDA events) the three calls run one after another on one
-    stream, with the time recorded before and after each."""
+def capture_steps(bench, steps, start, events=None):
+    """One CUDA graph of `steps` consecutive steps (replica (start + i) % R).  The
+    new block's compression runs on a second stream beside the indexer (which does
+    not read the compressed cache); attention waits for both.  With `events`
+    ([step][calls + 1] CUDA events) the calls run one after another on one stream
+    with an event recorded before and after each."""
     g = torch.cuda.CUDAGraph()
     s = torch.cuda.Stream()
     side = torch.cuda.Stream()
@@ -289,25 +418,95 @@ def capture_block(bench, steps, start, events=None):
         for i in range(steps):
             r = (start + i) % bench.R
             if events is not None:
-                events[i][0].record()
+                ev = events[i]
+                ev[0].record()
                 bench.compress(r)
-                events[i][1].record()
-                bench.index(r)
-                events[i][2].record()
+                ev[1].record()
+                if bench.wl.kind == "csa":
+                    bench.index(r)
+                    ev[2].record()
                 bench.attn(r)
-                events[i][3].record()
+                ev[-1].record()
                 continue
-            fork, join = torch.cuda.Event(), torch.cuda.Event()
-            fork.record(s)
-            side.wait_event(fork)
-            with torch.cuda.stream(side):
+            if bench.wl.kind == "csa":
+                fork, join = torch.cuda.Event(), torch.cuda.Event()
+                fork.record(s)
+                side.wait_event(fork)
+                with torch.cuda.stream(side):
+                    bench.compress(r)
+                join.record(side)
+                bench.index(r)
+                s.wait_event(join)
+            else:
                 bench.compress(r)
-            join.record(side)
-            bench.index(r)
-            s.wait_event(join)
             bench.attn(r)
     torch.cuda.current_stream().wait_stream(s)
     return g
+
+
+def time_decode(bench, K: int, W: int, block: int, ws: int, min_repeat_s: float = 1.0):
+    """Exactly K steps timed once (barrier + synchronize on both sides, max over
+    ranks), then the same K steps replayed at least 20 times (and for at least
+    `min_repeat_s`), each replay timed alone; returns both and the replay median."""
+    for i in range(max(W, 3)):  # eager warm-up (also sets kernel attributes before any capture)
+        bench.step(i % bench.R)
+    torch.cuda.synchronize()
+    graphs = []
+    done = 0
+    while done < K:
+        n = min(block, K - done)
+        graphs.append(capture_steps(bench, n, done % bench.R))
+        done += n
+
+    def replay_all():
+        for g in graphs:
+            g.replay()
+
+    for _ in range(max(1, math.ceil(max(W, 3) / K))):  # graph warm-up: at least W steps
+        replay_all()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    barrier(ws)
+    torch.cuda.synchronize()
+    t0.record()
+    replay_all()
+    t1.record()
+    torch.cuda.synchronize()
+    barrier(ws)
+    ms_total = max_over_ranks(t0.elapsed_time(t1), ws)
+    reps = []
+    wall0 = time.perf_counter()
+    while len(reps) < 20 or time.perf_counter() - wall0 < min_repeat_s:
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        replay_all()
+        e1.record()
+        e1.synchronize()
+        reps.append(e0.elapsed_time(e1) / K)
+        if len(reps) >= 100000:
+            break
+    med = max_over_ranks(statistics.median(reps), ws)
+    return {"ms_per_step": ms_total / K, "ms_per_step_median": med, "replays": len(reps),
+            "ms_per_step_min": min(reps), "ms_per_step_max": max(reps)}
+
+
+def per_call_ms(bench, steps: int = 64, reps: int = 4) -> dict:
+    """Device time of each call of the step: the steps replayed with an event
+    record between the calls (those nodes add ~1-2 us per call, so the step time
+    comes from the uninstrumented graphs)."""
+    n = len(bench.calls) + 1
+    ev = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(n)] for _ in range(steps)]
+    g = capture_steps(bench, steps, 0, ev)
+    acc = {c: [] for c in bench.calls}
+    for _ in range(reps):
+        g.replay()
+        torch.cuda.synchronize()
+        for i in range(steps):
+            for c, name in enumerate(bench.calls):
+                acc[name].append(ev[i][c].elapsed_time(ev[i][c + 1]))
+    return {k: statistics.fmean(v) for k, v in acc.items()}
 
 
 def time_graph(fn, R: int, steps: int = 64, reps: int = 20) -> float:
@@ -337,24 +536,10 @@ def time_state_append(bench, steps: int = 64, reps: int = 20) -> float:
     B, N, d = wl.B, wl.N, wl.d
     st_k = torch.zeros((B, d), dtype=torch.float32, device=bench.dev)
     st_v = torch.zeros_like(st_k)
-    kn, vn = bench.k_raw[:, N - 1:N], bench.v_raw[:, N - 1:N]
     pos = bench.ctx - 1
-    g = torch.cuda.CUDAGraph()
-    s = torch.cuda.Stream()
-    s.wait_stream(torch.cuda.current_stream())
-    with torch.cuda.graph(g, stream=s):
-        for _ in range(steps):
-            L.hsa_compress_append(kn, vn, pos, bench.w, wl.m, st_k, st_v, bench.kc, bench.vc)
-    torch.cuda.current_stream().wait_stream(s)
-    g.replay()
-    torch.cuda.synchronize()
-    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    t0.record()
-    for _ in range(reps):
-        g.replay()
-    t1.record()
-    torch.cuda.synchronize()
-    return t0.elapsed_time(t1) / (reps * steps)
+    return time_graph(lambda r: L.hsa_compress_append(bench.k_raw[r][:, N - 1:N], bench.v_raw[r][:, N - 1:N], pos,
+                                                      bench.w, wl.m, st_k, st_v, bench.kc[r], bench.vc[r]),
+                      bench.R, steps, reps)
 
 
 def time_v4_details(bench, steps: int = 64, reps: int = 20) -> dict:
@@ -372,127 +557,104 @@ def time_v4_details(bench, steps: int = 64, reps: int = 20) -> dict:
     sink = torch.zeros(H, device=dev)
     out = bench.out[0].clone()
     lse = torch.zeros((B, H), dtype=torch.float32, device=dev)
-    kc = bench.kc.clone()
+    kc = bench.kc[0].clone()
     calls = {
-        "v4_prep_query": lambda: L.hsa_rmsnorm_rope(q.view(B, 1, H, d), zeros, ones, 1, pos, 1, 0, gamma),
-        "v4_prep_entry": lambda: L.hsa_rmsnorm_rope(kc, E_new - 1, E_new, 1, None, m, m - 1, gamma),
-        "v4_finalize": lambda: L.hsa_attn_finalize(out, lse, pos, sink),
+        "v4_prep_query": lambda r: L.hsa_rmsnorm_rope(q.view(B, 1, H, d), zeros, ones, 1, pos, 1, 0, gamma),
+        "v4_prep_entry": lambda r: L.hsa_rmsnorm_rope(kc, E_new - 1, E_new, 1, None, m, m - 1, gamma),
+        "v4_finalize": lambda r: L.hsa_attn_finalize(out, lse, pos, sink),
     }
-    res = {}
-    for name, fn in calls.items():
-        g = torch.cuda.CUDAGraph()
-        s = torch.cuda.Stream()
-        s.wait_stream(torch.cuda.current_stream())
-        with torch.cuda.graph(g, stream=s):
-            for _ in range(steps):
-                fn()
-        torch.cuda.current_stream().wait_stream(s)
-        g.replay()
-        torch.cuda.synchronize()
-        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        t0.record()
-        for _ in range(reps):
-            g.replay()
-        t1.record()
-        torch.cuda.synchronize()
-        res[name] = t0.elapsed_time(t1) / (reps * steps)
-    return res
+    return {name: time_graph(fn, 1, steps, reps) for name, fn in calls.items()}
+
+
+def decode_row(wl, bench, t, op_ms, ws):
+    """JSON row of one decode workload: rate, bandwidth and roofline fractions."""
+    peak, peak_kind = load_peaks()
+    ms = t["ms_per_step"]
+    by = algorithmic_bytes(wl, bench.ctx_host.tolist(), bench.cnt_total())
+    row = {"workload": wl.name, "queries_per_s": wl.B * ws / (ms * 1e-3), "ms_per_step": ms,
+           "ms_per_step_median": t["ms_per_step_median"], "replays": t["replays"],
+           "algorithmic_bytes_per_step": by["step"], "hbm_gbs_step": by["step"] / (ms * 1e-3) / 1e9,
+           "step_frac_of_hbm": by["step"] / (ms * 1e-3) / 1e9 / peak,
+           "step_frac_of_hbm_median": by["step"] / (t["ms_per_step_median"] * 1e-3) / 1e9 / peak,
+           "peak_gbs": peak, "peak_source": peak_kind, "op_ms": op_ms,
+           "l2": f"{bench.R} rotating replicas of every per-step buffer, {bench.R * bench.replica_bytes() / 2**30:.1f} GiB"}
+    for call in ("index_topk", "attn_decode"):
+        if call in op_ms and by[call]:
+            ach = by[call] / (op_ms[call] * 1e-3) / 1e9
+            row[f"{call}_gbs"] = ach
+            row[f"{call}_frac_of_hbm"] = ach / peak
+    return row
+
+
+def run_decode(args, ws, rank, local, name, replicas):
+    dev = torch.device("cuda", local)
+    wl = WORKLOADS[name]
+    bench = DecodeBench(wl, replicas, 1000 * wl.wid + 100 * rank, dev)
+    t = time_decode(bench, args.steps, args.warmup, args.block, ws)
+    op_ms = per_call_ms(bench, steps=min(64, max(8, args.block)))
+    row = decode_row(wl, bench, t, op_ms, ws)
+    return row, bench
 
 
 def run_hsa(args, ws, rank, local):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    R, BLOCK = args.replicas, args.block
-    bench = DecodeBench(WL, R, 1000 * WL.wid + 100 * rank, dev)
-    # eager warm-up (also sets kernel attributes before any capture)
-    for i in range(max(args.warmup, 3)):
-        bench.step(i % R)
-    torch.cuda.synchronize()
-
-    K = args.steps
-    nblk, tail = divmod(K, BLOCK)
-    g_main = capture_block(bench, BLOCK, 0)
-    g_tail = capture_block(bench, tail, (nblk * BLOCK) % R) if tail else None
-    # graph warm-up
-    for _ in range(max(1, args.warmup // BLOCK)):
-        g_main.replay()
-    torch.cuda.synchronize()
-
-    t0 = torch.cuda.Event(enable_timing=True)
-    t1 = torch.cuda.Event(enable_timing=True)
+    wl = WORKLOADS[HEADLINE]
     sampler = ClockSampler(local)
-    barrier(ws)
-    torch.cuda.synchronize()
     with sampler:
-        t0.record()
-        for _ in range(nblk):
-            g_main.replay()
-        if g_tail is not None:
-            g_tail.replay()
-        t1.record()
-        torch.cuda.synchronize()
-    barrier(ws)
-    ms_total = t0.elapsed_time(t1)
-    ms_total = max_over_ranks(ms_total, ws)
-    ms_step = ms_total / K
-
-    # Per-op device time: the same steps replayed with an event record node
-    # between the calls (the nodes themselves add a little time per step, so the
-    # step time above comes from the uninstrumented graph).
-    ev = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(4)] for _ in range(BLOCK)]
-    g_ev = capture_block(bench, BLOCK, 0, ev)
-    per_op = {"compress": [], "index_topk": [], "attn_decode": []}
-    reps = max(1, min(8, nblk))
-    for _ in range(reps):
-        g_ev.replay()
-        torch.cuda.synchronize()
-        for i in range(BLOCK):
-            per_op["compress"].append(ev[i][0].elapsed_time(ev[i][1]))
-            per_op["index_topk"].append(ev[i][1].elapsed_time(ev[i][2]))
-            per_op["attn_decode"].append(ev[i][2].elapsed_time(ev[i][3]))
-    op_ms = {k: statistics.fmean(v) for k, v in per_op.items()}
+        head, bench = run_decode(args, ws, rank, local, HEADLINE, args.replicas)
+    op_ms = head["op_ms"]
     op_ms["compress_append"] = time_state_append(bench)
     op_ms.update(time_v4_details(bench))
-    op_ms["attn_decode_shared_kv"] = time_graph(lambda r: bench.L.hsa_attn_decode(
-        bench.q[r], bench.kc, bench.kc, WL.m, bench.idx[r].view(WL.B, WL.topk), bench.cnt[r].view(WL.B),
-        bench.k_raw, bench.k_raw, WL.window, bench.ctx, WL.scale, bench.out[r], bench.lse[r], bench.ws_a), bench.R)
-
-    cnt_total = int(sum(int(c.sum()) for c in bench.cnt[:1]))
-    bytes_ = algorithmic_bytes(WL, cnt_total)
+    op_ms["attn_decode_shared_kv"] = time_graph(lambda r: bench.attn(r, kv_shared=True), bench.R)
+    by = algorithmic_bytes(wl, bench.ctx_host.tolist(), bench.cnt_total())
     peak, peak_kind = load_peaks()
-    queries = WL.B * ws
-    value = queries / (ms_step * 1e-3)
-
-    # end to end through the public API: pinned host inputs in, result out, every step
-    e2e = None if args.profile else run_e2e(bench, args, dev)
-
+    ms_step = head["ms_per_step"]
+    queries = wl.B * ws
+    e2e = None if args.profile else run_e2e(bench, args)
+    ach = by["index_topk"] / (op_ms["index_topk"] * 1e-3) / 1e9
     out = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": K, "warmup": args.warmup,
-        "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16 (int8 indexer, int32 scores, fp32 accumulate)", "data": "synthetic (seeded N(0,1) bf16, uniform int8)",
-        "config": {"workload": WL.name, "global_batch": WL.B * ws, "seq_len": WL.N, "parallelism": f"replicas x{ws}",
-                   "l2": f"rotating {R} input replicas: {R * WL.B * (WL.N // WL.m) * WL.DI / 2**20:.0f} MiB of indexer keys > 4x L2",
-                   "graph_block": BLOCK},
-        "hbm_gbs_step": bytes_["step"] / (ms_step * 1e-3) / 1e9,
-        "gpu_launches": KERNELS_PER_STEP * K,
+        "metric": METRIC, "value": queries / (ms_step * 1e-3), "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16 (int8 indexer, int32 scores, fp32 accumulate)",
+        "data": "synthetic (seeded N(0,1) bf16, uniform int8)",
+        "config": {"workload": wl.name, "global_batch": wl.B * ws, "seq_len": wl.N,
+                   "parallelism": f"replicas x{ws}" if ws > 1 else "one GPU",
+                   "l2": head["l2"] + " (> 4x L2: inputs larger than L2, no flush)",
+                   "graph_block": args.block},
+        "value_median_of_replays": queries / (head["ms_per_step_median"] * 1e-3),
+        "ms_per_step_median_of_replays": head["ms_per_step_median"], "replays": head["replays"],
+        "hbm_gbs_step": head["hbm_gbs_step"],
+        "gpu_launches": len(bench.calls) * args.steps,
         "e2e": e2e,
+        "roofline": {"kernel": "index_fused_kernel (hsa_index_topk; one launch per step)", "bound": "hbm",
+                     "achieved": ach, "peak": peak, "unit": "GB/s", "frac": ach / peak,
+                     "traffic": args.traffic if args.traffic is not None
+                     else measured_traffic("index_fused_kernel", HEADLINE),
+                     "peak_source": peak_kind, "algorithmic_bytes_per_launch": by["index_topk"],
+                     "duration": "mean per-call device time of the step's calls replayed with events between them"},
+        "step_roofline": {"bound": "hbm", "achieved": head["hbm_gbs_step"], "peak": peak, "unit": "GB/s",
+                          "frac": head["step_frac_of_hbm"], "frac_median_of_replays": head["step_frac_of_hbm_median"],
+                          "algorithmic_bytes_per_step": by["step"]},
+        "op_ms": op_ms,
+        "clocks": sampler.summary(),
     }
-    if op_ms["index_topk"]:
-        ach = bytes_["index_topk"] / (op_ms["index_topk"] * 1e-3) / 1e9
-        out["roofline"] = {"kernel": "index_fused_kernel (hsa_index_topk; one launch per step)", "bound": "hbm",
-                           "achieved": ach, "peak": peak, "unit": "GB/s", "frac": ach / peak,
-                           "traffic": args.traffic if args.traffic is not None else index_traffic(),
-                           "peak_source": peak_kind,
-                           "algorithmic_bytes_per_launch": bytes_["index_topk"]}
-        step_ach = bytes_["step"] / (ms_step * 1e-3) / 1e9
-        out["step_roofline"] = {"bound": "hbm", "achieved": step_ach, "peak": peak, "unit": "GB/s",
-                                "frac": step_ach / peak, "algorithmic_bytes_per_step": bytes_["step"]}
-        out["op_ms"] = op_ms
-    out["clocks"] = sampler.summary()
-    return out, bench
+    del bench
+    torch.cuda.empty_cache()
+    rows = {}
+    for name in args.decode_rows:
+        s2 = ClockSampler(local)
+        with s2:
+            row, b2 = run_decode(args, ws, rank, local, name, args.replicas)
+        row["clocks"] = s2.summary()
+        rows[name] = row
+        del b2
+        torch.cuda.empty_cache()
+    out["decode_rows"] = rows
+    return out
 
 
-def run_e2e(bench, args, dev):
+def run_e2e(bench, args):
     """Same metric through the Python/C-ABI calls with host buffers: each step copies
     its inputs (q, indexer query) from pinned host memory, runs the three calls, reads
     the output back to pinned host memory, and waits for it.  The step's copies and
@@ -524,12 +686,10 @@ def run_e2e(bench, args, dev):
                 bench.compress(r)
             join.record(side)
             dqi.copy_(hqi[r], non_blocking=True)
-        bench.L.hsa_index_topk(dqi, bench.ki[r], bench.pos0, wl.m, wl.topk, bench.idx[r], bench.cnt[r], bench.ws_i)
+        bench.index(r, qi=dqi)
         if side is not None:
             torch.cuda.current_stream().wait_event(join)
-        bench.L.hsa_attn_decode(dq, bench.kc, bench.vc, wl.m, bench.idx[r].view(wl.B, wl.topk), bench.cnt[r].view(wl.B),
-                                bench.k_raw, bench.v_raw, wl.window, bench.ctx, wl.scale, bench.out[r], bench.lse[r],
-                                bench.ws_a)
+        bench.attn(r, q=dq)
         hout.copy_(bench.out[r], non_blocking=True)
 
     def timed(one):
@@ -573,13 +733,19 @@ def run_e2e(bench, args, dev):
 
 # --------------------------------------------------- chunked prefill rows
 
-def prefill_flops(wl) -> float:
-    """4*H*d FLOP per (query row, attended item): QK^T and PV, multiply-add = 2 FLOP."""
+def prefill_items(wl, rows=None):
+    """Attended items per query row (selected or visible entries + window)."""
     p = np.arange(wl.N - wl.T, wl.N, dtype=np.int64)
+    if rows is not None:
+        p = p[rows]
     E = (p + 1) // wl.m
     sel = np.minimum(E, wl.topk) if wl.kind == "csa" else E
-    items = sel + np.minimum(wl.window, p + 1)
-    return 4.0 * wl.B * wl.H * wl.d * float(items.sum())
+    return sel + np.minimum(wl.window, p + 1)
+
+
+def prefill_flops(wl, rows=None) -> float:
+    """4*H*d FLOP per (query row, attended item): QK^T and PV, multiply-add = 2 FLOP."""
+    return 4.0 * wl.B * wl.H * wl.d * float(prefill_items(wl, rows).sum())
 
 
 def run_prefill(dev, reps: int):
@@ -590,7 +756,6 @@ def run_prefill(dev, reps: int):
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
     peak_tc = load_peaks(kind="bf16_tflops")
-    peak_bw, _ = load_peaks()
 
     def timed(fn):
         ts = []
@@ -633,6 +798,7 @@ def run_prefill(dev, reps: int):
         r["compress_learned_chunk_ms"] = timed(lambda: L.hsa_compress_learned(kr, vr, pos0, full, T // m, u_l, b_l, m,
                                                                               kc, vc))
         idx = cnt = None
+        macs = 0.0
         if wl.kind == "csa":
             qi = torch.randint(-127, 128, (B, T, wl.DI), generator=g, device=dev, dtype=torch.int16).to(torch.int8)
             ki = torch.randint(-127, 128, (B, E, wl.DI), generator=g, device=dev, dtype=torch.int16).to(torch.int8)
@@ -673,30 +839,32 @@ def run_prefill(dev, reps: int):
 
 # ------------------------------------------------------ oracle (CPU) arm
 
-def oracle_sample_setup(seconds_hint=True):
-    """One sequence of the workload on the host, its compressed cache built by the oracle."""
+def oracle_sample_setup():
+    """One sequence of the headline workload on the host, its compressed cache built by the oracle."""
     import oracle
     from compressed_attention_compress_b300.inputs import bf16_bits, make_inputs
     oracle.build()
-    x = make_inputs(WL, B=1)
-    m = WL.m
-    E = WL.N // m
+    wl = WORKLOADS[HEADLINE]
+    x = make_inputs(wl, B=1)
+    m = wl.m
+    E = wl.N // m
     kr, vr = bf16_bits(x.k_raw), bf16_bits(x.v_raw)
-    kc = oracle.compress(kr, x.w.numpy(), m, [0], [WL.N], E, out_dtype=np.float32)
-    vc = oracle.compress(vr, x.w.numpy(), m, [0], [WL.N], E, out_dtype=np.float32)
+    kc = oracle.compress(kr, x.w.numpy(), m, [0], [wl.N], E, out_dtype=np.float32)
+    vc = oracle.compress(vr, x.w.numpy(), m, [0], [wl.N], E, out_dtype=np.float32)
     return oracle, x, kr, vr, kc, vc
 
 
-def oracle_query(oracle, x, kr, vr, kc, vc, rep: int):
+def oracle_query(oracle, x, kr, vr, kc, vc):
     """One decode query through the oracle: compress the new block, index + top-k, attention."""
     from compressed_attention_compress_b300.inputs import bf16_bits
-    m, N = WL.m, WL.N
+    wl = WORKLOADS[HEADLINE]
+    m, N = wl.m, wl.N
     p = N - 1
     newblk = oracle.compress(kr[:, N - m:], x.w.numpy(), m, [0], [m], 1, out_dtype=np.float32)
     kc[:, -1] = newblk[:, 0]
-    oi, oc = oracle.index_topk_rows(x.q_idx.numpy().reshape(1, WL.DI), [0], [p], x.k_idx.numpy(), m, WL.topk)
-    o, l = oracle.attn_rows(bf16_bits(x.q).reshape(1, WL.H, WL.d), [0], [p], kc, vc, m, oi, kr, vr, WL.window,
-                            WL.scale)
+    oi, oc = oracle.index_topk_rows(x.q_idx.numpy().reshape(1, wl.DI), [0], [p], x.k_idx.numpy(), m, wl.topk)
+    o, l = oracle.attn_rows(bf16_bits(x.q).reshape(1, wl.H, wl.d), [0], [p], kc, vc, m, oi, kr, vr, wl.window,
+                            wl.scale)
     return o
 
 
@@ -708,7 +876,7 @@ def cpu_baseline(budget_s: float):
     n = 0
     t = time.perf_counter()
     while True:
-        oracle_query(oracle, x, kr, vr, kc, vc, n)
+        oracle_query(oracle, x, kr, vr, kc, vc)
         n += 1
         if time.perf_counter() - t >= budget_s:
             break
@@ -719,40 +887,94 @@ def cpu_baseline(budget_s: float):
             "cpu": platform.processor() or platform.machine()}
 
 
+def cpu_baseline_prefill(budget_s: float):
+    """The oracle on a row sample of each chunked-prefill layer: for the CSA layer,
+    indexer + top-k + attention of single query rows; for the HCA layer, attention of
+    single query rows.  Rows are taken every 512th from the chunk's start, one at a
+    time, until `budget_s` per layer; the rate is reported in query rows/s and in the
+    attention's TFLOP/s (4*H*d FLOP per attended item)."""
+    import oracle
+    from compressed_attention_compress_b300.inputs import bf16_bits, make_inputs
+    oracle.build()
+    res = {}
+    for name in ("prefill_hca", "prefill_csa"):
+        wl = WORKLOADS[name]
+        x = make_inputs(wl)
+        m, T, N = wl.m, wl.T, wl.N
+        E = N // m
+        kr, vr = bf16_bits(x.k_raw), bf16_bits(x.v_raw)
+        kc = oracle.compress(kr, x.w.numpy(), m, [0], [N], E, out_dtype=np.float32)
+        vc = oracle.compress(vr, x.w.numpy(), m, [0], [N], E, out_dtype=np.float32)
+        qb = bf16_bits(x.q.reshape(T, wl.H, wl.d))
+        done = []
+        t = time.perf_counter()
+        for row in range(0, T, 512):
+            p = N - T + row
+            oi = None
+            if wl.kind == "csa":
+                oi, _ = oracle.index_topk_rows(x.q_idx.numpy().reshape(T, wl.DI)[row:row + 1], [0], [p],
+                                               x.k_idx.numpy(), m, wl.topk)
+            oracle.attn_rows(qb[row:row + 1], [0], [p], kc, vc, m, oi, kr, vr, wl.window, wl.scale)
+            done.append(row)
+            if time.perf_counter() - t >= budget_s:
+                break
+        dt = time.perf_counter() - t
+        flop = prefill_flops(wl, np.array(done))
+        res[name] = {"value": len(done) / dt, "unit": "query rows/s", "tflops": flop / dt / 1e12,
+                     "cores": oracle.num_threads(), "kind": "oracle",
+                     "sample": f"{len(done)} query rows (every 512th of the 8192-token chunk), {dt:.1f} s"}
+        del x, kr, vr, kc, vc
+    return res
+
+
 def run_reference(args, ws, rank):
     if rank != 0:
         return None
     oracle, x, kr, vr, kc, vc = oracle_sample_setup()
-    for i in range(args.warmup if args.warmup < 3 else 3):
-        oracle_query(oracle, x, kr, vr, kc, vc, i)
+    for _ in range(min(args.warmup, 3)):
+        oracle_query(oracle, x, kr, vr, kc, vc)
     K = args.steps
-    # each step is one decode query (one of the B sequences' worth of work); bound the run to minutes
-    per = None
+    wl = WORKLOADS[HEADLINE]
     t = time.perf_counter()
     done = 0
-    for i in range(K):
-        oracle_query(oracle, x, kr, vr, kc, vc, i)
+    for _ in range(K):
+        oracle_query(oracle, x, kr, vr, kc, vc)
         done += 1
-        el = time.perf_counter() - t
-        per = el / done
-        if el > args.ref_budget:
+        if time.perf_counter() - t > args.ref_budget:
             break
     dt = time.perf_counter() - t
     value = done / dt
     return {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": done,
             "warmup": args.warmup, "ms_per_step": dt / done * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64 (oracle)", "data": "synthetic",
-            "config": {"workload": WL.name, "global_batch": 1, "seq_len": WL.N, "parallelism": "host cores"},
+            "config": {"workload": wl.name, "global_batch": 1, "seq_len": wl.N, "parallelism": "host cores"},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
                              "sample": f"{done} of the {K} requested steps, one decode query each (sequence 0); "
                                        f"run bounded to {args.ref_budget:.0f} s"},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
-def main():
+def run_dry(args, ws, rank):
+    """Launcher self-check without a GPU: every rank joins the process group, times a
+    trivial host loop, and rank 0 reports the max over ranks (tests the multi-rank
+    plumbing of this script on CPU ranks)."""
+    barrier(ws)
+    t = time.perf_counter()
+    acc = 0
+    for i in range(args.steps):
+        acc += i
+    dt = max_over_ranks(time.perf_counter() - t, ws)
+    barrier(ws)
+    if rank == 0:
+        return {"impl": "dry-run", "n_gpus": ws, "steps": args.steps, "seconds_max_over_ranks": dt,
+                "world_size": ws}
+    return None
+
+
+def parse(argv):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=64)
     ap.add_argument("--impl", choices=["hsa", "reference"], default="hsa")
     ap.add_argument("--replicas", type=int, default=8)
@@ -765,37 +987,49 @@ def main():
     ap.add_argument("--prefill-reps", type=int, default=10)
     ap.add_argument("--prefill-only", action="store_true",
                     help="only the chunked-prefill rows (for profiling their kernels)")
+    ap.add_argument("--decode-rows", default=",".join(EXTRA_DECODE),
+                    help="comma-separated extra decode workloads timed beside the headline")
     ap.add_argument("--profile", action="store_true",
-                    help="small run for ncu captures: 2 replicas, no end-to-end or CPU legs")
-    args = ap.parse_args()
+                    help="small run for ncu captures: 2 replicas, no end-to-end, CPU or extra legs")
+    ap.add_argument("--dry-run", action="store_true", help="launcher self-check on CPU ranks (no GPU work)")
+    args = ap.parse_args(argv)
+    args.decode_rows = [r for r in args.decode_rows.split(",") if r]
     if args.profile:
         args.replicas, args.block, args.no_cpu_baseline = 2, max(1, min(args.block, args.steps)), True
-        args.no_prefill = True
-    # the oracle's host threads are started before any GPU work
-    ws, rank, local = dist_setup(args)
-    if args.impl == "reference":
-        res = run_reference(args, ws, rank)
-        if res is not None:
+        args.no_prefill, args.decode_rows = True, []
+    return args
+
+
+def main(argv=None):
+    argv = sys.argv[1:] if argv is None else argv
+    args = parse(argv)
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        spawn_ranks(argv, args.gpus)
+        return
+    ws, rank, local = dist_setup()
+    try:
+        if args.dry_run:
+            res = run_dry(args, ws, rank)
+        elif args.impl == "reference":
+            res = run_reference(args, ws, rank)
+        elif args.prefill_only:
+            torch.cuda.set_device(local)
+            res = {"prefill": run_prefill(torch.device("cuda", local), args.prefill_reps)}
+        else:
+            res = run_hsa(args, ws, rank, local)
+            torch.cuda.empty_cache()
+            if not args.no_prefill:
+                res["prefill"] = run_prefill(torch.device("cuda", local), args.prefill_reps)
+            if rank == 0 and not args.no_cpu_baseline and ws == 1:
+                res["cpu_baseline"] = cpu_baseline(args.cpu_budget)
+                res["prefill"] = res.get("prefill") or {}
+                res["prefill"]["cpu_baseline"] = cpu_baseline_prefill(args.cpu_budget / 2)
+        if rank == 0 and res is not None:
             print(json.dumps(res), flush=True)
-        return
-    if args.prefill_only:
-        torch.cuda.set_device(local)
-        res = run_prefill(torch.device("cuda", local), args.prefill_reps)
-        if rank == 0:
-            print(json.dumps({"prefill": res}), flush=True)
-        return
-    res, bench = run_hsa(args, ws, rank, local)
-    del bench
-    torch.cuda.empty_cache()
-    if not args.no_prefill:
-        res["prefill"] = run_prefill(torch.device("cuda", local), args.prefill_reps)
-    if rank == 0:
-        if not args.no_cpu_baseline and ws == 1:
-            res["cpu_baseline"] = cpu_baseline(args.cpu_budget)
-        print(json.dumps(res), flush=True)
-    if ws > 1:
-        import torch.distributed as dist
-        dist.destroy_process_group()
+    finally:
+        if ws > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
 
 
 if __name__ == "__main__":
