@@ -93,6 +93,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, unsigned parity) {
         : "memory");
     return ok != 0;
 }
+// Non-blocking test of an mbarrier phase (never suspends the thread: for polling
+// loops that watch several barriers).
+__device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, unsigned parity) {
+    unsigned ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
 // Bounded wait on an mbarrier phase; false if it gave up.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, unsigned parity, unsigned long long limit = 1ull << 22) {
     for (unsigned long long i = 0; i < limit; ++i)

@@ -96,10 +96,62 @@ __global__ void __launch_bounds__(256) compress_kernel(CompressArgs a) {
     }
 }
 
+// Few long blocks (HCA, m = 128, one block per sequence in a decode step): one CTA
+// per (block, sequence, K or V) copies the block's m rows into shared memory with
+// every 16-byte load in flight at once, then each thread folds its channels over
+// r = 0..m-1 with the same fmaf sequence as compress_kernel (bit-identical
+// entries), instead of one thread walking the m rows one load group at a time.
+template <typename T>
+__global__ void __launch_bounds__(128) compress_staged_kernel(CompressArgs a) {
+    extern __shared__ __align__(16) unsigned char s_raw[];
+    float *s_w = reinterpret_cast<float *>(s_raw);
+    T *s_x = reinterpret_cast<T *>(s_raw + ((a.m * sizeof(float) + 15) & ~(size_t)15));
+    const int b = blockIdx.y;
+    const bool is_v = blockIdx.z == 1;
+    const int64_t j = a.tok_begin[b] / a.m + blockIdx.x;
+    if (j >= a.tok_end[b] / a.m) return;
+    if (a.tok_begin[b] < 0 || (j + 1) * a.m > a.N_cap || j >= a.E_cap) {
+        if (threadIdx.x == 0) raise_flag(FLAG_COMPRESS_RANGE);
+        return;
+    }
+    const T *x = static_cast<const T *>(is_v ? a.v : a.k) + b * a.in_sb + j * a.m * a.in_st;
+    const int cpr = a.d * (int)sizeof(T) / 16;  // 16-byte chunks per row
+    for (int i = threadIdx.x; i < a.m * cpr; i += blockDim.x) {
+        const int r = i / cpr, c = i - r * cpr;
+        cp_async_16(smem_u32(reinterpret_cast<unsigned char *>(s_x) + (size_t)i * 16),
+                    reinterpret_cast<const unsigned char *>(x + r * a.in_st) + c * 16, 16);
+    }
+    cp_async_commit();
+    for (int r = threadIdx.x; r < a.m; r += blockDim.x) s_w[r] = a.w[r];
+    cp_async_wait<0>();
+    __syncthreads();
+    T *out = static_cast<T *>(is_v ? a.vc : a.kc) + b * a.out_sb + j * a.out_se;
+    for (int e = threadIdx.x; e < a.d; e += blockDim.x) {
+        float acc = 0.f;
+#pragma unroll 8
+        for (int r = 0; r < a.m; ++r) acc = fmaf(s_w[r], load_elem(s_x + (size_t)r * a.d + e), acc);
+        store_elem(out + e, acc);
+    }
+}
+
 cudaError_t launch_compress(const CompressArgs &a, bool bf16, int num_sms, cudaStream_t s) {
     const int V = bf16 ? 8 : 4;
     const int64_t total = a.max_blocks * (a.d / V) * a.B;
     if (total <= 0) return cudaSuccess;
+    const size_t staged = ((a.m * sizeof(float) + 15) & ~(size_t)15) + (size_t)a.m * a.d * (bf16 ? 2 : 4);
+    if (a.m >= 16 && staged <= 96 * 1024 && a.max_blocks * a.B <= 8ll * num_sms && a.max_blocks <= 65535 &&
+        a.B <= 65535) {
+        static unsigned long long done_bf16 = 0, done_f32 = 0;
+        cudaError_t e = bf16 ? smem_limit_once(compress_staged_kernel<__nv_bfloat16>, 96 * 1024, done_bf16)
+                             : smem_limit_once(compress_staged_kernel<float>, 96 * 1024, done_f32);
+        if (e != cudaSuccess) return e;
+        const dim3 grid((unsigned)a.max_blocks, (unsigned)a.B, 2);
+        if (bf16)
+            compress_staged_kernel<__nv_bfloat16><<<grid, 128, staged, s>>>(a);
+        else
+            compress_staged_kernel<float><<<grid, 128, staged, s>>>(a);
+        return cudaGetLastError();
+    }
     const int threads = 256;
     int64_t want = (total + threads - 1) / threads;
     const int64_t cap = (int64_t)num_sms * 8;

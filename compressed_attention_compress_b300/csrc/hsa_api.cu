@@ -147,6 +147,16 @@ DecodePlan plan_decode(hsa_dtype_t dt, int B, int H, int d, int64_t E_cap, int m
         p.total = w.total;
         return p;
     }
+    if (dt == HSA_BF16 && dense && hsa::decode_dense_tc_shape(B, H, d)) {
+        // tcgen05 dense kernel: one partial per 128-item tile, merged in tile order
+        const hsa::DecodeDenseWorkspace w = hsa::decode_dense_workspace(B, H, E_cap, window);
+        p.split = -2;
+        p.max_splits = 1;
+        p.off_o = w.off_o;
+        p.off_lse = w.off_ml;
+        p.total = w.total;
+        return p;
+    }
     if (dt == HSA_BF16 && hsa::decode_cluster_supported(H, d)) {
         p.split = -1;  // cluster kernel: splits live in one cluster, no workspace
         p.max_splits = 1;
@@ -464,6 +474,7 @@ hsa_status_t hsa_attn_decode(const void *q, hsa_dtype_t dt, int B, int H, int d,
     a.part_o = p.total ? reinterpret_cast<float *>(static_cast<char *>(ws) + p.off_o) : nullptr;
     a.part_lse = p.total ? reinterpret_cast<float *>(static_cast<char *>(ws) + p.off_lse) : nullptr;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (p.split == -2) return launched(hsa::launch_attn_decode_dense_tc(a, di.num_sms, s), "attn_decode (tcgen05 dense)");
     if (p.split < 0) {
         if (hsa::decode_tc_supported(a)) return launched(hsa::launch_attn_decode_tc(a, s), "attn_decode (tcgen05)");
         return launched(hsa::launch_attn_decode_cluster(a, s), "attn_decode (cluster)");

@@ -192,6 +192,15 @@ struct DecodeTcWorkspace {
 DecodeTcWorkspace decode_tc_workspace(int B, int H, int topk, int window);
 bool decode_tc_supported(const AttnArgs &a);
 cudaError_t launch_attn_decode_tc(const AttnArgs &a, cudaStream_t s);
+// bf16 dense (HCA) decode with d = 128, H a multiple of 64, B <= 1024: one unit per
+// 128-item tile of each (sequence, 64-head group), persistent tcgen05 + TMA kernel, the
+// tiles' partials (part_o: O, part_lse: maximum and sum) merged in tile order.
+bool decode_dense_tc_shape(int B, int H, int d);
+struct DecodeDenseWorkspace {
+    size_t off_o, off_ml, off_cum, total;  // part_o at off_o, part_lse at off_ml, tile prefix at off_cum
+};
+DecodeDenseWorkspace decode_dense_workspace(int B, int H, int64_t E_cap, int window);
+cudaError_t launch_attn_decode_dense_tc(const AttnArgs &a, int num_sms, cudaStream_t s);
 // bf16 dense (HCA) prefill with d = 128 and T*H a multiple of 128: tcgen05 + TMA kernel.
 bool prefill_tc_supported(const AttnArgs &a);
 cudaError_t launch_attn_prefill_tc(const AttnArgs &a, int num_sms, cudaStream_t s);

@@ -243,8 +243,12 @@ HSA_API hsa_status_t hsa_index_topk_noalloc(const int8_t *q_idx, int64_t q_sb, i
  * with logits scale * <q[b,h], k_x> and one softmax; out[b, h] is the
  * softmax-weighted sum of v_x and lse[b, h] its natural-log normaliser
  * (-inf and out = 0 for an empty set).  Work is split over the set and the
- * parts are combined with the log-sum-exp rule; the split count of a
- * sequence depends only on its own set size.
+ * parts are combined with the log-sum-exp rule.  CSA (idx given): the split of
+ * a sequence depends only on its own set size, so its output is bit-identical
+ * whatever else is in the batch.  HCA (idx == NULL), bf16, d = 128, H a
+ * multiple of 64, B <= 1024: the batch's 128-item tiles are split evenly over
+ * the SMs, so outputs are deterministic for a given batch but may differ in the
+ * last bits from the same sequence decoded in another batch.
  *   q          [B, H, d] of `dt`, contiguous
  *   kc, vc     [B, E_cap, d] of `dt`, strides (c_sb, c_se)
  *   idx, cnt   int32 [B, topk] (ascending or not; entries < 0 are skipped)
@@ -258,7 +262,9 @@ HSA_API hsa_status_t hsa_index_topk_noalloc(const int8_t *q_idx, int64_t q_sb, i
  *              multiple of 64 and topk + window <= 2048 the parts are tiles of
  *              128 slots, one thread-block cluster per (sequence, 64 heads), and
  *              the workspace holds their fp32 partials, about B * H/64 *
- *              ceil((topk + window) / 128) * 33,280 bytes.
+ *              ceil((topk + window) / 128) * 33,280 bytes; for bf16 HCA
+ *              (d = 128, H a multiple of 64) about B * H/64 * (ceil(E_cap / 128)
+ *              + ceil(window / 128)) * 33,280 bytes.
  * Every pointer is a device pointer; host memory, pinned or not, is refused
  * with HSA_ERR_INVALID_ARG before anything is enqueued.
  * bf16: d in {64, 128}, H a multiple of 16 up to 128.  fp32: d a multiple of
