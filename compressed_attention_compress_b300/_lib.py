@@ -23,7 +23,7 @@ _STATUS = {0: "HSA_OK", 1: "HSA_ERR_INVALID_ARG", 2: "HSA_ERR_UNSUPPORTED", 3: "
 
 # every symbol include/hsa.h declares
 EXPORTS = ["hsa_last_error", "hsa_version", "hsa_check", "hsa_check_pointer", "hsa_compress", "hsa_compress_append", "hsa_compress_learned", "hsa_index_topk_workspace_size",
-           "hsa_index_topk", "hsa_index_topk_noalloc", "hsa_attn_decode_workspace_size", "hsa_attn_decode",
+           "hsa_index_topk", "hsa_index_topk_noalloc", "hsa_attn_decode_workspace_size", "hsa_attn_decode", "hsa_decode_csa_workspace_size", "hsa_decode_csa",
            "hsa_attn_prefill_workspace_size", "hsa_attn_prefill", "hsa_index_scores", "hsa_topk_merge",
            "hsa_lse_merge", "hsa_rmsnorm_rope", "hsa_attn_finalize"]
 NOALLOC_SCRATCH_BYTES = 16 << 20
@@ -64,6 +64,11 @@ def _load():
     lib.hsa_attn_decode.restype = I
     lib.hsa_attn_decode.argtypes = [P, I, I, I, I, P, P, I64, I64, I64, I, P, P, I, P, P, I64, I64, I64, I, P, F,
                                     P, P, P, SZ, P]
+    lib.hsa_decode_csa_workspace_size.restype = I
+    lib.hsa_decode_csa_workspace_size.argtypes = [I, I, I, I, I64, ctypes.POINTER(SZ)]
+    lib.hsa_decode_csa.restype = I
+    lib.hsa_decode_csa.argtypes = [P, I64, P, I64, I64, I64, I, I, I, P, P, P, I, I, I, I, P, P, I64, I64, P, P, I64,
+                                   I64, I64, I, P, F, P, P, P, SZ, P]
     lib.hsa_attn_prefill_workspace_size.restype = I
     lib.hsa_attn_prefill_workspace_size.argtypes = [I, I, I, I, I, I64, I, I, I, ctypes.POINTER(SZ)]
     lib.hsa_attn_prefill.restype = I
@@ -187,6 +192,27 @@ def hsa_attn_decode(q, kc, vc, m, idx, cnt, k_raw, v_raw, window, ctx_len, scale
                              int(m), _p(idx), _p(cnt), topk, _p(k_raw), _p(v_raw), k_raw.stride(0), k_raw.stride(1),
                              k_raw.shape[1], int(window), _p(ctx_len), float(scale), _p(out), _p(lse), _p(ws),
                              ws.numel() * ws.element_size() if ws is not None else 0, _stream(stream)))
+
+
+def hsa_decode_csa_workspace_size(B, H, d, DI, E_cap):
+    n = ctypes.c_size_t(0)
+    _chk(lib.hsa_decode_csa_workspace_size(B, H, d, DI, E_cap, ctypes.byref(n)))
+    return n.value
+
+
+def hsa_decode_csa(q_idx, k_idx, m, topk, idx_out, cnt_out, q, kc, vc, k_raw, v_raw, window, ctx_len, scale, out,
+                   lse=None, ws=None, stream=None):
+    """One CSA decode step: q_idx int8 [B, DI] (or [B, 1, DI]); k_idx int8 [B, E_cap, DI]; idx_out int32
+    [B, topk]; cnt_out int32 [B]; q [B, H, d]; kc/vc [B, E_cap, d]; out [B, H, d]; lse fp32 [B, H]."""
+    B, H, d = q.shape
+    qi = q_idx.reshape(B, -1)
+    DI = qi.shape[1]
+    E_cap = k_idx.shape[1]
+    _chk(lib.hsa_decode_csa(_p(qi), qi.stride(0), _p(k_idx), k_idx.stride(0), k_idx.stride(1), E_cap, DI, int(m),
+                            int(topk), _p(idx_out), _p(cnt_out), _p(q), _dt(q), B, H, d, _p(kc), _p(vc), kc.stride(0),
+                            kc.stride(1), _p(k_raw), _p(v_raw), k_raw.stride(0), k_raw.stride(1), k_raw.shape[1],
+                            int(window), _p(ctx_len), float(scale), _p(out), _p(lse), _p(ws),
+                            ws.numel() * ws.element_size() if ws is not None else 0, _stream(stream)))
 
 
 def hsa_attn_prefill_workspace_size(dtype, B, T, H, d, E_cap, m, topk, window):

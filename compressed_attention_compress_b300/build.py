@@ -9,7 +9,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 ROOT = os.path.dirname(HERE)
 LIB = os.path.join(HERE, "libhsa.so")
-SOURCES = ["hsa_api.cu", "compress.cu", "index_topk.cu", "index_fused.cu", "attn.cu", "attn_decode_cluster.cu", "attn_prefill_tc.cu", "index_prefill_tc.cu", "cp_merge.cu", "v4_extras.cu", "attn_gather_tc.cu", "attn_decode_tc.cu", "attn_decode_dense_tc.cu"]
+SOURCES = ["hsa_api.cu", "compress.cu", "index_topk.cu", "index_fused.cu", "attn.cu", "attn_decode_cluster.cu", "attn_prefill_tc.cu", "index_prefill_tc.cu", "cp_merge.cu", "v4_extras.cu", "attn_gather_tc.cu", "attn_decode_tc.cu", "attn_decode_dense_tc.cu", "decode_fused.cu"]
 HEADERS = ["common.cuh", "internal.h", "block_scan.cuh", "tc_common.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -484,6 +484,72 @@ hsa_status_t hsa_attn_decode(const void *q, hsa_dtype_t dt, int B, int H, int d,
     return launched(hsa::launch_attn_merge(a, dt == HSA_BF16, s), "attn_merge");
 }
 
+hsa_status_t hsa_decode_csa_workspace_size(int B, int H, int d, int DI, int64_t E_cap, size_t *bytes) {
+    if (!bytes) return fail(HSA_ERR_INVALID_ARG, "null bytes");
+    if (B < 0 || H <= 0 || d <= 0 || DI <= 0 || E_cap < 0) return fail(HSA_ERR_INVALID_ARG, "bad size");
+    if (B == 0) {
+        *bytes = 0;
+        return ok();
+    }
+    DevInfo di;
+    hsa_status_t st = device_info(di);
+    if (st != HSA_OK) return st;
+    if (d != 128) return fail(HSA_ERR_UNSUPPORTED, "hsa_decode_csa needs d = 128, got %d", d);
+    const hsa::DecodeStepPlan pl = hsa::plan_decode_step(B, H, DI, E_cap, di.num_sms);
+    if (!pl.ok)
+        return fail(HSA_ERR_UNSUPPORTED, "hsa_decode_csa: B=%d H=%d DI=%d E_cap=%lld does not fit one resident launch "
+                    "(use hsa_index_topk and hsa_attn_decode)", B, H, DI, (long long)E_cap);
+    *bytes = pl.total;
+    return ok();
+}
+
+hsa_status_t hsa_decode_csa(const int8_t *q_idx, int64_t qi_sb, const int8_t *k_idx, int64_t k_sb, int64_t k_se,
+                            int64_t E_cap, int DI, int m, int topk, int32_t *idx_out, int32_t *cnt_out, const void *q,
+                            hsa_dtype_t dt, int B, int H, int d, const void *kc, const void *vc, int64_t c_sb,
+                            int64_t c_se, const void *k_raw, const void *v_raw, int64_t r_sb, int64_t r_st,
+                            int64_t N_cap, int window, const int64_t *ctx_len, float scale, void *out, float *lse,
+                            void *ws, size_t ws_bytes, hsa_stream_t stream) {
+    if (B < 0 || H <= 0 || d <= 0 || DI <= 0 || E_cap < 0 || m <= 0 || window < 0 || N_cap < 0)
+        return fail(HSA_ERR_INVALID_ARG, "bad size");
+    if (dt != HSA_BF16 || d != 128 || (H != 64 && H != 128))
+        return fail(HSA_ERR_UNSUPPORTED, "hsa_decode_csa needs bf16, d = 128 and H in {64, 128}");
+    if (topk <= 0 || topk > 4096) return fail(HSA_ERR_UNSUPPORTED, "topk must be in [1, 4096], got %d", topk);
+    if (DI != 16 && DI != 32 && DI != 64 && DI != 128)
+        return fail(HSA_ERR_UNSUPPORTED, "indexer dim must be 16, 32, 64 or 128, got %d", DI);
+    if (B == 0) return ok();
+    if (B > 65535) return fail(HSA_ERR_UNSUPPORTED, "more than 65535 sequences");
+    if (E_cap == 0) return fail(HSA_ERR_UNSUPPORTED, "no compressed entries: use hsa_attn_decode");
+    if (E_cap > (int64_t)1 << 30) return fail(HSA_ERR_UNSUPPORTED, "E_cap above 2^30");
+    if (!q_idx || !k_idx || !idx_out || !cnt_out || !q || !kc || !vc || !ctx_len || !out)
+        return fail(HSA_ERR_INVALID_ARG, "null pointer");
+    if (window > 0 && (!k_raw || !v_raw)) return fail(HSA_ERR_INVALID_ARG, "null raw cache with window > 0");
+    if (k_se != DI) return fail(HSA_ERR_UNSUPPORTED, "hsa_decode_csa needs contiguous indexer rows (k_se == DI)");
+    if (!aligned16(q_idx) || !aligned16(k_idx) || qi_sb % 16 || k_sb % 16)
+        return fail(HSA_ERR_UNSUPPORTED, "indexer tensors and strides must be 16-byte aligned");
+    if (!aligned16(q) || !aligned16(out) || !aligned16(kc) || !aligned16(vc) || (k_raw && !aligned16(k_raw)) ||
+        (v_raw && !aligned16(v_raw)))
+        return fail(HSA_ERR_UNSUPPORTED, "q, out and caches must be 16-byte aligned");
+    if (c_sb % 8 || c_se % 8 || r_sb % 8 || r_st % 8) return fail(HSA_ERR_UNSUPPORTED, "cache strides must be multiples of 16 bytes");
+    if (c_se < d || r_st < d || c_sb < 0 || r_sb < 0) return fail(HSA_ERR_INVALID_ARG, "cache strides overlap rows");
+    DevInfo di;
+    hsa_status_t st = device_info(di);
+    if (st != HSA_OK) return st;
+    const hsa::DecodeStepPlan pl = hsa::plan_decode_step(B, H, DI, E_cap, di.num_sms);
+    if (!pl.ok)
+        return fail(HSA_ERR_UNSUPPORTED, "hsa_decode_csa: B=%d H=%d DI=%d E_cap=%lld does not fit one resident launch "
+                    "(use hsa_index_topk and hsa_attn_decode)", B, H, DI, (long long)E_cap);
+    if (!ws || ws_bytes < pl.total) return fail(HSA_ERR_WORKSPACE, "decode workspace needs %zu bytes, got %zu", pl.total, ws_bytes);
+    if ((reinterpret_cast<uintptr_t>(ws) & 255) != 0) return fail(HSA_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+    if ((st = check_pointers({{q_idx, "q_idx"}, {k_idx, "k_idx"}, {idx_out, "idx_out"}, {cnt_out, "cnt_out"}, {q, "q"},
+                              {kc, "kc"}, {vc, "vc"}, {k_raw, "k_raw"}, {v_raw, "v_raw"}, {ctx_len, "ctx_len"},
+                              {out, "out"}, {lse, "lse"}, {ws, "workspace"}})) != HSA_OK)
+        return st;
+    if ((st = pending_error()) != HSA_OK) return st;
+    hsa::DecodeStepCall c{q_idx, qi_sb, k_idx, k_sb, E_cap, B, DI, m, topk, H, window, idx_out, cnt_out, q, kc, vc,
+                          k_raw, v_raw, c_sb, c_se, r_sb, r_st, N_cap, ctx_len, scale, out, lse};
+    return launched(hsa::launch_decode_step(c, pl, ws, reinterpret_cast<cudaStream_t>(stream)), "decode_csa");
+}
+
 hsa_status_t hsa_attn_prefill_workspace_size(hsa_dtype_t dt, int B, int T, int H, int d, int64_t E_cap, int m,
                                              int topk, int window, size_t *bytes) {
     (void)dt; (void)B; (void)T; (void)H; (void)d; (void)E_cap; (void)m; (void)topk; (void)window;

@@ -83,6 +83,31 @@ struct FusedIndexPlan {
 FusedIndexPlan plan_index_fused(int rows, int DI, int64_t E_cap, int num_sms);
 cudaError_t launch_index_fused(const IndexArgs &a, const FusedIndexPlan &p, void *ws, cudaStream_t s);
 
+// One CSA decode step (indexer, exact top-k, attention) in one cooperative launch
+// (decode_fused.cu): bf16, d = 128, H in {64, 128}, indexer keys contiguous.
+struct DecodeStepPlan {
+    bool ok;
+    int rows, ctas_per_row, chunk, key_bits, shift1, nb2;
+    size_t smem;
+    size_t off_hist, off_bar, off_rec, off_b1, off_po, off_pml, zero_bytes, total;
+};
+DecodeStepPlan plan_decode_step(int B, int H, int DI, int64_t E_cap, int num_sms);
+struct DecodeStepCall {
+    const int8_t *qi;
+    int64_t qi_sb;
+    const int8_t *ki;
+    int64_t ki_sb, E_cap;
+    int B, DI, m, topk, H, window;
+    int32_t *idx_out, *cnt_out;
+    const void *q, *kc, *vc, *k_raw, *v_raw;
+    int64_t c_sb, c_se, r_sb, r_st, N_cap;
+    const int64_t *ctx;
+    float scale;
+    void *out;
+    float *lse;
+};
+cudaError_t launch_decode_step(const DecodeStepCall &c, const DecodeStepPlan &p, void *ws, cudaStream_t s);
+
 // Many-row indexer on tcgen05 tensor cores (index_prefill_tc.cu).
 struct PrefillIndexPlan {
     bool ok;

@@ -280,6 +280,40 @@ HSA_API hsa_status_t hsa_attn_decode(const void *q, hsa_dtype_t dt, int B, int H
                              void *out, float *lse, void *ws, size_t ws_bytes, hsa_stream_t stream);
 
 /*
+ * hsa_decode_csa -- one CSA decode step in one launch: the indexer and exact
+ * top-k of hsa_index_topk followed by the attention of hsa_attn_decode over the
+ * selected entries plus the window (QbitAI article, 混合注意力机制: CSA steps 2
+ * and 3 and the sliding-window paragraph).  For sequence b with its query at
+ * p = ctx_len[b] - 1 (so q_pos0 = ctx_len - 1 for the indexer):
+ *   idx_out[b, :], cnt_out[b]   exactly as hsa_index_topk (bit-identical)
+ *   out[b, h], lse[b, h]        as hsa_attn_decode with idx = idx_out, cnt = cnt_out
+ * The CTAs that score a sequence's entries also attend to the entries they
+ * select and meet at three barriers inside one cooperative launch, instead of
+ * a grid-wide hand-off between two kernels.  The split of the attention follows
+ * the launch's chunks, which depend on B: outputs are deterministic for a given
+ * batch (not bit-identical across batches).
+ *   q_idx      int8 [B, DI], row stride qi_sb;  k_idx int8 [B, E_cap, DI] with
+ *              k_se == DI (contiguous rows), sequence stride k_sb
+ *   idx_out    int32 [B, topk];  cnt_out int32 [B]
+ *   q          [B, H, d] bf16 contiguous;  kc, vc [B, E_cap, d] (c_sb, c_se);
+ *              k_raw, v_raw [B, N_cap, d] (r_sb, r_st);  out [B, H, d];  lse [B, H]
+ *              fp32 or NULL
+ *   ws         workspace of hsa_decode_csa_workspace_size bytes, zero-filled
+ *              once before first use (left zero by every call)
+ * bf16, d = 128, H in {64, 128}, DI in {16, 32, 64, 128}, 1 <= topk <= 4096,
+ * E_cap >= 1.  Sizes whose chunks cannot all be resident at once return
+ * HSA_ERR_UNSUPPORTED (use the two calls).
+ */
+HSA_API hsa_status_t hsa_decode_csa_workspace_size(int B, int H, int d, int DI, int64_t E_cap, size_t *bytes);
+HSA_API hsa_status_t hsa_decode_csa(const int8_t *q_idx, int64_t qi_sb, const int8_t *k_idx, int64_t k_sb,
+                                    int64_t k_se, int64_t E_cap, int DI, int m, int topk, int32_t *idx_out,
+                                    int32_t *cnt_out, const void *q, hsa_dtype_t dt, int B, int H, int d,
+                                    const void *kc, const void *vc, int64_t c_sb, int64_t c_se, const void *k_raw,
+                                    const void *v_raw, int64_t r_sb, int64_t r_st, int64_t N_cap, int window,
+                                    const int64_t *ctx_len, float scale, void *out, float *lse, void *ws,
+                                    size_t ws_bytes, hsa_stream_t stream);
+
+/*
  * hsa_attn_prefill -- T query tokens per sequence at positions
  * q_pos0[b] .. q_pos0[b]+T-1, each with its own set S as in hsa_attn_decode
  * (causal within the chunk through E(p) and the window bound; the raw cache

@@ -82,6 +82,34 @@ def test_decode_workload(lib, name):
     assert_close_lse(lse, rl)
 
 
+@pytest.mark.parametrize("name", ["flash_csa_decode", "pro_csa_decode"])
+def test_decode_step_workload(lib, name):
+    # the one-launch decode step on the full-size decode workloads
+    wl = WORKLOADS[name]
+    x = make_inputs(wl)
+    dev = torch.device("cuda", 0)
+    B, N, H, d, m = wl.B, wl.N, wl.H, wl.d, wl.m
+    E = N // m
+    kr, vr, kc, vc = _gpu_cache(lib, x, dev)
+    idx = torch.empty((B, wl.topk), dtype=torch.int32, device=dev)
+    cnt = torch.empty((B,), dtype=torch.int32, device=dev)
+    out = torch.empty((B, H, d), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((B, H), dtype=torch.float32, device=dev)
+    ws = lib.workspace(lib.hsa_decode_csa_workspace_size(B, H, d, wl.DI, E), device=dev)
+    lib.hsa_decode_csa(x.q_idx.to(dev), x.k_idx.to(dev), m, wl.topk, idx, cnt, x.q.to(dev), kc, vc, kr, vr,
+                       wl.window, x.ctx_len.to(dev), wl.scale, out, lse, ws)
+    lib.hsa_check()
+    rows_p = (x.ctx_len - 1).numpy()
+    oidx, ocnt = oracle.index_topk_rows(x.q_idx.numpy(), np.arange(B), rows_p, x.k_idx.numpy(), m, wl.topk)
+    assert np.array_equal(cnt.cpu().numpy(), ocnt)
+    assert np.array_equal(idx.cpu().numpy(), oidx)
+    okc, ovc = _oracle_cache(x, E, x.ctx_len.numpy())
+    ro, rl = oracle.attn_rows(bf16_bits(x.q), np.arange(B), rows_p, okc, ovc, m, oidx, bf16_bits(x.k_raw),
+                              bf16_bits(x.v_raw), wl.window, wl.scale)
+    assert_close_out(out, ro, torch.bfloat16)
+    assert_close_lse(lse, rl)
+
+
 def _sample_rows(T):
     """Rows whose outputs are compared on long chunks: every 16th, the first 64 and the last 64."""
     rows = set(range(min(64, T))) | set(range(max(0, T - 64), T)) | set(range(0, T, 16))
