@@ -308,7 +308,7 @@ def spawn_ranks(argv, n: int):
 class DecodeBench:
     """Device buffers of R input replicas and the C-ABI calls of one decode step."""
 
-    def __init__(self, wl, replicas: int, seed_base: int, dev):
+    def __init__(self, wl, replicas: int, seed_base: int, dev, fused: bool = False):
         from compressed_attention_compress_b300 import _lib as L
         self.L, self.wl, self.dev, self.R = L, wl, dev, replicas
         B, N, H, d, m = wl.B, wl.N, wl.H, wl.d, wl.m
@@ -365,8 +365,22 @@ class DecodeBench:
         self.ws_a = L.workspace(L.hsa_attn_decode_workspace_size(torch.bfloat16, B, H, d, E, m,
                                                                  wl.topk if wl.kind == "csa" else 0, wl.window),
                                 device=dev)
+        # CSA: the one-launch decode step (hsa_decode_csa) when the shape fits it, else
+        # the two calls hsa_index_topk + hsa_attn_decode
+        self.fused = False
+        if wl.kind == "csa" and fused:
+            try:
+                self.ws_f = L.workspace(L.hsa_decode_csa_workspace_size(B, H, d, wl.DI, E), device=dev)
+                self.fused = True
+            except L.HSAError:
+                self.fused = False
         torch.cuda.synchronize(dev)
-        self.calls = ("compress", "index_topk", "attn_decode") if wl.kind == "csa" else ("compress", "attn_decode")
+        if self.fused:
+            self.calls = ("compress", "decode_step")
+        elif wl.kind == "csa":
+            self.calls = ("compress", "index_topk", "attn_decode")
+        else:
+            self.calls = ("compress", "attn_decode")
 
     def replica_bytes(self) -> int:
         per = sum(t.numel() * t.element_size() for t in (self.k_raw[0], self.v_raw[0], self.kc[0], self.vc[0]))
@@ -392,8 +406,18 @@ class DecodeBench:
                                self.cnt[r].view(wl.B) if csa else None, self.k_raw[r], vr, wl.window, self.ctx,
                                wl.scale, self.out[r], self.lse[r], self.ws_a)
 
+    def decode_step(self, r, qi=None, q=None):
+        wl = self.wl
+        self.L.hsa_decode_csa(self.qi[r] if qi is None else qi, self.ki[r], wl.m, wl.topk,
+                              self.idx[r].view(wl.B, wl.topk), self.cnt[r].view(wl.B), self.q[r] if q is None else q,
+                              self.kc[r], self.vc[r], self.k_raw[r], self.v_raw[r], wl.window, self.ctx, wl.scale,
+                              self.out[r], self.lse[r], self.ws_f)
+
     def step(self, r):
         self.compress(r)
+        if self.fused:
+            self.decode_step(r)
+            return
         if self.wl.kind == "csa":
             self.index(r)
         self.attn(r)
@@ -405,9 +429,10 @@ class DecodeBench:
 
 
 def capture_steps(bench, steps, start, events=None):
-    """One CUDA graph of `steps` consecutive steps (replica (start + i) % R).  The
-    new block's compression runs on a second stream beside the indexer (which does
-    not read the compressed cache); attention waits for both.  With `events`
+    """One CUDA graph of `steps` consecutive steps (replica (start + i) % R).  With
+    the one-launch decode step the new block's compression runs first (the step
+    reads the compressed cache); with two calls it runs on a second stream beside
+    the indexer (which does not read it) and the attention waits for both.  With `events`
     ([step][calls + 1] CUDA events) the calls run one after another on one stream
     with an event recorded before and after each."""
     g = torch.cuda.CUDAGraph()
@@ -422,11 +447,19 @@ def capture_steps(bench, steps, start, events=None):
                 ev[0].record()
                 bench.compress(r)
                 ev[1].record()
+                if bench.fused:
+                    bench.decode_step(r)
+                    ev[-1].record()
+                    continue
                 if bench.wl.kind == "csa":
                     bench.index(r)
                     ev[2].record()
                 bench.attn(r)
                 ev[-1].record()
+                continue
+            if bench.fused:
+                bench.compress(r)
+                bench.decode_step(r)
                 continue
             if bench.wl.kind == "csa":
                 fork, join = torch.cuda.Event(), torch.cuda.Event()
@@ -578,18 +611,21 @@ def decode_row(wl, bench, t, op_ms, ws):
            "step_frac_of_hbm_median": by["step"] / (t["ms_per_step_median"] * 1e-3) / 1e9 / peak,
            "peak_gbs": peak, "peak_source": peak_kind, "op_ms": op_ms,
            "l2": f"{bench.R} rotating replicas of every per-step buffer, {bench.R * bench.replica_bytes() / 2**30:.1f} GiB"}
-    for call in ("index_topk", "attn_decode"):
+    by["decode_step"] = by["index_topk"] + by["attn_decode"]
+    for call in ("index_topk", "attn_decode", "decode_step"):
         if call in op_ms and by[call]:
             ach = by[call] / (op_ms[call] * 1e-3) / 1e9
             row[f"{call}_gbs"] = ach
             row[f"{call}_frac_of_hbm"] = ach / peak
+    row["path"] = "hsa_decode_csa (one launch)" if bench.fused else (
+        "hsa_index_topk + hsa_attn_decode" if wl.kind == "csa" else "hsa_attn_decode")
     return row
 
 
-def run_decode(args, ws, rank, local, name, replicas):
+def run_decode(args, ws, rank, local, name, replicas, fused=False):
     dev = torch.device("cuda", local)
     wl = WORKLOADS[name]
-    bench = DecodeBench(wl, replicas, 1000 * wl.wid + 100 * rank, dev)
+    bench = DecodeBench(wl, replicas, 1000 * wl.wid + 100 * rank, dev, fused=fused)
     t = time_decode(bench, args.steps, args.warmup, args.block, ws)
     op_ms = per_call_ms(bench, steps=min(64, max(8, args.block)))
     row = decode_row(wl, bench, t, op_ms, ws)
@@ -612,7 +648,14 @@ def run_hsa(args, ws, rank, local):
     ms_step = head["ms_per_step"]
     queries = wl.B * ws
     e2e = None if args.profile else run_e2e(bench, args)
-    ach = by["index_topk"] / (op_ms["index_topk"] * 1e-3) / 1e9
+    if bench.fused:
+        kname, call = "decode_step_kernel", "decode_step"
+        kbytes = by["index_topk"] + by["attn_decode"]
+        kdesc = "decode_step_kernel (hsa_decode_csa: indexer, top-k and attention; one launch per step)"
+    else:
+        kname, call, kbytes = "index_fused_kernel", "index_topk", by["index_topk"]
+        kdesc = "index_fused_kernel (hsa_index_topk; one launch per step)"
+    ach = kbytes / (op_ms[call] * 1e-3) / 1e9
     out = {
         "metric": METRIC, "value": queries / (ms_step * 1e-3), "unit": UNIT, "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
@@ -627,11 +670,10 @@ def run_hsa(args, ws, rank, local):
         "hbm_gbs_step": head["hbm_gbs_step"],
         "gpu_launches": len(bench.calls) * args.steps,
         "e2e": e2e,
-        "roofline": {"kernel": "index_fused_kernel (hsa_index_topk; one launch per step)", "bound": "hbm",
+        "roofline": {"kernel": kdesc, "bound": "hbm",
                      "achieved": ach, "peak": peak, "unit": "GB/s", "frac": ach / peak,
-                     "traffic": args.traffic if args.traffic is not None
-                     else measured_traffic("index_fused_kernel", HEADLINE),
-                     "peak_source": peak_kind, "algorithmic_bytes_per_launch": by["index_topk"],
+                     "traffic": args.traffic if args.traffic is not None else measured_traffic(kname, HEADLINE),
+                     "peak_source": peak_kind, "algorithmic_bytes_per_launch": kbytes,
                      "duration": "mean per-call device time of the step's calls replayed with events between them"},
         "step_roofline": {"bound": "hbm", "achieved": head["hbm_gbs_step"], "peak": peak, "unit": "GB/s",
                           "frac": head["step_frac_of_hbm"], "frac_median_of_replays": head["step_frac_of_hbm_median"],
@@ -642,12 +684,23 @@ def run_hsa(args, ws, rank, local):
     del bench
     torch.cuda.empty_cache()
     rows = {}
-    for name in args.decode_rows:
+    # the decode rows through the two calls, and the CSA ones also through the
+    # one-launch step (hsa_decode_csa) where its plan fits the shape
+    todo = [(name, False) for name in args.decode_rows]
+    if not args.profile:
+        todo += [(name, True) for name in [HEADLINE] + list(args.decode_rows) if WORKLOADS[name].kind == "csa"]
+    for name, fused in todo:
+        key = name + ("_one_launch" if fused else "")
         s2 = ClockSampler(local)
         with s2:
-            row, b2 = run_decode(args, ws, rank, local, name, args.replicas)
-        row["clocks"] = s2.summary()
-        rows[name] = row
+            row, b2 = run_decode(args, ws, rank, local, name, args.replicas, fused=fused)
+        if fused and not b2.fused:
+            rows[key] = {"workload": WORKLOADS[name].name,
+                         "unsupported": "hsa_decode_csa: the shape does not fit one resident launch "
+                                        "(TMEM-using kernels are resident one CTA per SM)"}
+        else:
+            row["clocks"] = s2.summary()
+            rows[key] = row
         del b2
         torch.cuda.empty_cache()
     out["decode_rows"] = rows
@@ -672,6 +725,26 @@ def run_e2e(bench, args):
     steps = max(20, min(args.steps, 2000))
 
     def calls(r, side=None):
+        if bench.fused:
+            # the step reads the compressed cache: compress, then the one-launch step; the
+            # query copies travel on the second stream beside the compression
+            if side is None:
+                dq.copy_(hq[r], non_blocking=True)
+                dqi.copy_(hqi[r], non_blocking=True)
+                bench.compress(r)
+            else:
+                fork, join = torch.cuda.Event(), torch.cuda.Event()
+                fork.record()
+                side.wait_event(fork)
+                with torch.cuda.stream(side):
+                    dq.copy_(hq[r], non_blocking=True)
+                    dqi.copy_(hqi[r], non_blocking=True)
+                join.record(side)
+                bench.compress(r)
+                torch.cuda.current_stream().wait_event(join)
+            bench.decode_step(r, qi=dqi, q=dq)
+            hout.copy_(bench.out[r], non_blocking=True)
+            return
         if side is None:
             dq.copy_(hq[r], non_blocking=True)
             dqi.copy_(hqi[r], non_blocking=True)

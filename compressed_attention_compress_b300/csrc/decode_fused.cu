@@ -22,10 +22,11 @@
 //       T and how many keys equal to T are taken (the first in index order), so
 //       it knows every chunk's number of winners and its own winners' places in
 //       the ascending output, which it writes.  It then runs the attention over
-//       its own winners (the row's last CTA adds the window) on the tensor cores
+//       its own winners and its share of the window on the tensor cores
 //       -- S = Q K^T with M = 128 query heads (H = 64 pads Q with zero rows) and
 //       N = 64 items, an online softmax, O += P V in TMEM -- and writes its
-//       partial (O in bf16, maximum, sum).                         -- barrier 3
+//       partial (O in bf16, maximum, sum).  The window tokens are dealt round
+//       robin over the row's CTAs.                                 -- barrier 3
 //   P4  every CTA combines a share of the heads over the row's partials with the
 //       log-sum-exp rule and writes the output and the log-sum-exp.
 // The histogram is cleared after barrier 2, the counters by the row's last CTA
@@ -42,7 +43,7 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kNB1 = 2048;                     // level-1 histogram bins
-constexpr int kStages = 4;                     // key-stream stages
+constexpr int kStages = 3;                     // key-stream stages
 constexpr int kStageBytes = 16384;
 constexpr int kM = 128;                        // MMA M: query heads (padded)
 constexpr int kD = 128;                        // head dim
@@ -51,8 +52,11 @@ constexpr int kQBlk = kM * 128;                // 16 KiB: one 64-column block of
 constexpr int kQBytes = 2 * kQBlk;             // 32 KiB
 constexpr int kTBlk = kNT * 128;               // 8 KiB: one 64-column block of a K or V tile
 constexpr int kTile = 2 * kTBlk;               // 16 KiB
-constexpr int kPBytes = kM * 128;              // 16 KiB: P [128 heads][64 items] bf16
-constexpr int kAttnBytes = kQBytes + 2 * kTile + kPBytes;  // 80 KiB
+// P [128 heads][64 items] bf16 (16 KiB) takes the K tile's place once S is done
+// (the V tile's when one buffer is both K and V)
+constexpr int kAttnBytes = kQBytes + 2 * kTile;  // 64 KiB
+constexpr int kWorkBytes = 16384 + kStages * kStageBytes;  // P1: histogram + stages (64 KiB)
+static_assert(kWorkBytes <= kAttnBytes, "the key stages fit the attention tiles' space");
 constexpr int kMaxChunks = 256;                // CTAs per row (one value per thread in the scans)
 constexpr unsigned long long kWaitNs = 200ull * 1000 * 1000;  // any wait gives up after 200 ms
 // device-flag bits of the wait that gave up (or the check that failed)
@@ -182,7 +186,7 @@ __device__ __forceinline__ void find_threshold(const unsigned *hist, int nb, int
 }
 
 template <int LPE>
-__global__ void __launch_bounds__(kThreads, 2) decode_step_kernel(StepArgs a, DecodeStepPlan p, void *ws) {
+__global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(StepArgs a, DecodeStepPlan p, void *ws) {
     extern __shared__ __align__(16) unsigned char smem_raw[];  // rounded up to 1024 at run time
     unsigned char *smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
     // [0, 80 KiB): P1 histogram (16 KiB) + key stages; P3 level-2 histogram; then
@@ -192,7 +196,8 @@ __global__ void __launch_bounds__(kThreads, 2) decode_step_kernel(StepArgs a, De
     unsigned char *s_stage = s_work + 16384;
     uint32_t *s_keys = reinterpret_cast<uint32_t *>(smem + kAttnBytes);
     int32_t *s_win = reinterpret_cast<int32_t *>(smem + kAttnBytes + (size_t)p.chunk * 4);
-    unsigned char *sQ = s_work, *sK = s_work + kQBytes, *sV = sK + kTile, *sP = sV + kTile;
+    // P takes the K tile's place once S is done (the V tile's when K and V are one buffer)
+    unsigned char *sQ = s_work, *sK = s_work + kQBytes, *sV = sK + kTile, *sP = a.shared_kv ? sV : sK;
     __shared__ int s_scan[33];
     __shared__ int s_misc[16];
     __shared__ int s_gt[kMaxChunks], s_eq[kMaxChunks];
@@ -437,15 +442,16 @@ __global__ void __launch_bounds__(kThreads, 2) decode_step_kernel(StepArgs a, De
         __syncthreads();
     }
 
-    // attention over this chunk's winners (the row's last chunk adds the window):
-    // 64-item tiles, one thread per head row of S and O (TMEM lane = head)
+    // attention over this chunk's winners and window tokens w_lo + c, w_lo + c + nch,
+    // ...: 64-item tiles, one thread per head row of S and O (TMEM lane = head)
     int64_t w_lo = 0;
     int n_wnd = 0;
-    if (c == nch - 1 && a.window > 0 && pos >= 0) {
+    if (a.window > 0 && pos >= 0) {
         w_lo = pos - a.window + 1 < 0 ? 0 : pos - a.window + 1;
-        n_wnd = (int)(pos - w_lo + 1);
+        const int n_all = (int)(pos - w_lo + 1);
+        n_wnd = c < n_all ? (n_all - c + nch - 1) / nch : 0;
         if (pos >= a.N_cap) {
-            if (tid == 0) raise_flag(FLAG_ATTN_RANGE);
+            if (tid == 0 && c == 0) raise_flag(FLAG_ATTN_RANGE);
             n_wnd = 0;
         }
     }
@@ -475,7 +481,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_step_kernel(StepArgs a, De
                 ks = a.kc + row * a.c_sb + e * a.c_se;
                 vs = a.vc + row * a.c_sb + e * a.c_se;
             } else if (item < n_items) {
-                const int64_t tk = w_lo + (item - n_win);
+                const int64_t tk = w_lo + c + (int64_t)(item - n_win) * nch;
                 ks = a.k_raw + row * a.r_sb + tk * a.r_st;
                 vs = a.v_raw + row * a.r_sb + tk * a.r_st;
             }
@@ -604,61 +610,75 @@ __global__ void __launch_bounds__(kThreads, 2) decode_step_kernel(StepArgs a, De
     ok = ok && row_barrier(&w.bar[0], 3u * (unsigned)nch, 2, &s_misc[15]);
 
     // ---------------------------------------------------------------- P4
-    // heads [c * hpc, (c + 1) * hpc) over the row's nch partials; warp: one head at a
-    // time, lane: columns 4l..4l+3
+    // heads [c * hpc, (c + 1) * hpc) over the row's nch partials, one head at a time
+    // by the whole CTA: warp g takes the partials g, g + 8, ... (all its loads in
+    // flight at once), lane l the columns 4l..4l+3; the warps' sums are added in
+    // warp order.
     if (ok) {
         const int hpc = (a.H + nch - 1) / nch;
         const int lane = tid & 31;
-        for (int h = c * hpc + warp; h < a.H && h < (c + 1) * hpc; h += kThreads / 32) {
-            float M = -INFINITY;
-            for (int i = lane; i < nch; i += 32) M = fmaxf(M, __ldcg(w.pml + (int64_t)i * 2 * a.H + h));
+        float *s_red = reinterpret_cast<float *>(s_work);  // [8][132]
+        for (int h = c * hpc; h < a.H && h < (c + 1) * hpc; ++h) {
+            float mv = -INFINITY;
+            for (int i = tid; i < nch; i += kThreads) mv = fmaxf(mv, __ldcg(w.pml + (int64_t)i * 2 * a.H + h));
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+            for (int o = 16; o > 0; o >>= 1) mv = fmaxf(mv, __shfl_xor_sync(0xffffffffu, mv, o));
+            if (lane == 0) s_red[warp * 132 + 128] = mv;
+            __syncthreads();
+            float M = -INFINITY;
+#pragma unroll
+            for (int g = 0; g < kThreads / 32; ++g) M = fmaxf(M, s_red[g * 132 + 128]);
             float L = 0.f, acc[4] = {0.f, 0.f, 0.f, 0.f};
             if (M != -INFINITY) {
-                for (int i0 = 0; i0 < nch; i0 += 32) {
-                    float wt = 0.f, lv = 0.f;
-                    if (i0 + lane < nch) {
-                        const float *pml = w.pml + (int64_t)(i0 + lane) * 2 * a.H;
-                        const float mv = __ldcg(pml + h);
-                        if (mv != -INFINITY) {
-                            wt = tc::ex2(mv - M);
-                            lv = __ldcg(pml + a.H + h);
+                constexpr int U = 16;
+                for (int i0 = warp; i0 < nch; i0 += U * (kThreads / 32)) {
+                    float m_[U], l_[U];
+                    uint2 ov[U];
+#pragma unroll
+                    for (int k = 0; k < U; ++k) {
+                        const int i = i0 + k * (kThreads / 32);
+                        m_[k] = -INFINITY;
+                        if (i < nch) {
+                            const float *pml = w.pml + (int64_t)i * 2 * a.H;
+                            m_[k] = __ldcg(pml + h);
+                            l_[k] = __ldcg(pml + a.H + h);
+                            ov[k] = __ldcg(reinterpret_cast<const uint2 *>(w.po + ((int64_t)i * a.H + h) * kD) + lane);
                         }
                     }
-                    const int cnt = nch - i0 < 32 ? nch - i0 : 32;
-                    constexpr int U = 8;
-                    for (int k0 = 0; k0 < cnt; k0 += U) {
-                        uint2 ov[U];
 #pragma unroll
-                        for (int k = 0; k < U; ++k) {
-                            const float wk = __shfl_sync(0xffffffffu, wt, (k0 + k) & 31);
-                            ov[k] = (k0 + k < cnt && wk != 0.f)
-                                        ? __ldcg(reinterpret_cast<const uint2 *>(
-                                                     w.po + ((int64_t)(i0 + k0 + k) * a.H + h) * kD) + lane)
-                                        : make_uint2(0u, 0u);
-                        }
-#pragma unroll
-                        for (int k = 0; k < U; ++k) {
-                            const float wk = __shfl_sync(0xffffffffu, wt, (k0 + k) & 31);
-                            const float lk = __shfl_sync(0xffffffffu, lv, (k0 + k) & 31);
-                            if (k0 + k >= cnt || wk == 0.f) continue;
-                            L = fmaf(wk, lk, L);
-                            acc[0] = fmaf(wk, bf16_lo(ov[k].x), acc[0]);
-                            acc[1] = fmaf(wk, bf16_hi(ov[k].x), acc[1]);
-                            acc[2] = fmaf(wk, bf16_lo(ov[k].y), acc[2]);
-                            acc[3] = fmaf(wk, bf16_hi(ov[k].y), acc[3]);
-                        }
+                    for (int k = 0; k < U; ++k) {
+                        if (m_[k] == -INFINITY) continue;  // nothing from that chunk (its O is not used)
+                        const float wk = tc::ex2(m_[k] - M);
+                        L = fmaf(wk, l_[k], L);
+                        acc[0] = fmaf(wk, bf16_lo(ov[k].x), acc[0]);
+                        acc[1] = fmaf(wk, bf16_hi(ov[k].x), acc[1]);
+                        acc[2] = fmaf(wk, bf16_lo(ov[k].y), acc[2]);
+                        acc[3] = fmaf(wk, bf16_hi(ov[k].y), acc[3]);
                     }
                 }
             }
-            const bool empty = !(L > 0.f);
-            const float inv = empty ? 0.f : 1.f / L;
-            uint2 pk;
-            pk.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
-            pk.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
-            *reinterpret_cast<uint2 *>(a.out + ((int64_t)row * a.H + h) * kD + lane * 4) = pk;
-            if (a.lse && lane == 0) a.lse[(int64_t)row * a.H + h] = empty ? -INFINITY : (M + log2f(L)) * kLn2;
+            __syncthreads();  // M read by every warp before the slots are reused
+#pragma unroll
+            for (int e = 0; e < 4; ++e) s_red[warp * 132 + 4 * lane + e] = acc[e];
+            if (lane == 0) s_red[warp * 132 + 129] = L;
+            __syncthreads();
+            if (warp == 0) {
+                float Lt = 0.f, o4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int g = 0; g < kThreads / 32; ++g) {
+                    Lt += s_red[g * 132 + 129];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) o4[e] += s_red[g * 132 + 4 * lane + e];
+                }
+                const bool empty = !(Lt > 0.f);
+                const float inv = empty ? 0.f : 1.f / Lt;
+                uint2 pk;
+                pk.x = pack_bf16x2(o4[0] * inv, o4[1] * inv);
+                pk.y = pack_bf16x2(o4[2] * inv, o4[3] * inv);
+                *reinterpret_cast<uint2 *>(a.out + ((int64_t)row * a.H + h) * kD + lane * 4) = pk;
+                if (a.lse && lane == 0) a.lse[(int64_t)row * a.H + h] = empty ? -INFINITY : (M + log2f(Lt)) * kLn2;
+            }
+            __syncthreads();
         }
     }
     // the row's last CTA out returns its counters to zero for the next call
@@ -721,12 +741,14 @@ DecodeStepPlan plan_decode_step(int B, int H, int DI, int64_t E_cap, int num_sms
     p.shift1 = p.key_bits - 11;
     p.nb2 = 1 << p.shift1;
     if (p.nb2 * 4 > 16384) return p;
-    // the smallest chunk (a multiple of 64 entries) whose launch is resident at once;
-    // at most two CTAs per SM, so that their TMEM (256 columns each) always fits
+    // the smallest chunk (a multiple of 64 entries) whose launch is resident at once
+    // (the occupancy query counts one CTA per SM for a kernel that allocates tensor
+    // memory)
     for (int chunk = 256; chunk <= 16384; chunk += 64) {
         const int64_t C = (E_cap + chunk - 1) / chunk;
         if (C > kMaxChunks) continue;
         const size_t smem = 1024 + (size_t)kAttnBytes + 2 * (size_t)chunk * 4;
+        if (smem > 200 * 1024) break;
         int occ = occupancy_for(DI, smem);
         if (occ <= 0) return p;
         if (occ > 2) occ = 2;

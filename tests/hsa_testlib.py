@@ -61,7 +61,8 @@ def gpu_index(q_idx, k_idx, q_pos0, m, topk, lib):
     idx = torch.empty((B, T, topk), dtype=torch.int32, device=q_idx.device)
     cnt = torch.empty((B, T), dtype=torch.int32, device=q_idx.device)
     ws = lib.workspace(lib.hsa_index_topk_workspace_size(B, T, DI, E_cap, topk), device=q_idx.device)
-    lib.hsa_index_topk(q_idx, k_idx, q_pos0.to(q_idx.device), m, topk, idx, cnt, ws)
+    for _ in range(2):  # twice on one workspace: each call must leave it ready for the next
+        lib.hsa_index_topk(q_idx, k_idx, q_pos0.to(q_idx.device), m, topk, idx, cnt, ws)
     return idx, cnt
 
 

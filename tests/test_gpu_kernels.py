@@ -145,6 +145,23 @@ def test_index_topk_concentrated_run(lib):
                 seed=seed)
 
 
+def test_index_topk_rising_scores(lib):
+    # scores rise with the index (312 equal entries per level): the top-k fill the
+    # last chunks, whose first candidates stop above the threshold bin, so every
+    # chunk rewrites its candidates before the selection; ties split by index
+    E_cap, DI, k, seed = 40000, 64, 1000, 13
+    q = _randint8((1, 1, DI), 100 + seed, -127, 127)
+    level = (torch.arange(E_cap) * 128 // E_cap).to(torch.int16)
+    kI = (torch.sign(q[0, 0].to(torch.int16))[None, :] * level[:, None]).to(torch.int8)[None]
+    _index_case(lib, B=1, T=1, E_cap=E_cap, DI=DI, m=4, topk=k, pos0=[4 * E_cap - 1], k_idx=kI, seed=seed)
+
+
+def test_index_topk_one_long_row(lib):
+    # one row of 2^18 entries: more chunks than threads in the selection phase
+    E_cap = 1 << 18
+    _index_case(lib, B=1, T=1, E_cap=E_cap, DI=64, m=4, topk=1024, pos0=[4 * E_cap - 1], seed=21)
+
+
 def test_index_topk_extreme_values(lib):
     # -128 everywhere: largest possible scores, all tied
     kI = torch.full((1, 5000, 64), -128, dtype=torch.int8)
