@@ -77,7 +77,7 @@ struct FusedIndexPlan {
     int rows, ctas_per_row, chunk, key_bits, shift1, nb2;
     int off_stage_smem;  // byte offset of the copy stages in dynamic shared memory
     size_t smem;
-    size_t off_hist1, off_bar, off_verd, off_rec, off_cut, off_cand, total;
+    size_t off_hist1, off_bar, off_rec, off_cand, total;
     size_t zero_bytes;   // the leading part that must be zero before a launch (histograms, counters)
 };
 FusedIndexPlan plan_index_fused(int rows, int DI, int64_t E_cap, int num_sms);
