@@ -61,12 +61,12 @@ UNIT = "queries/s"
 # that capture ran (sha256 of each file).
 TRAFFIC = {
     ("index_fused_kernel", "pro_csa_decode"): {
-        "bytes": 67258368 + 110336,
+        "bytes": 67262464 + 526080,
         "sources": {
             "compressed_attention_compress_b300/csrc/index_fused.cu":
-                "fd9e0083f6ed2eebb211bcb3ff11a3142598ba316ffa91176b925dcc9d2cf824",
+                "22b16b4e825f0b41d03a6b7665f415de88bb1082c1ea4179070ec70817a66404",
             "compressed_attention_compress_b300/csrc/common.cuh":
-                "1c50e4616466d69022320548d2a47c9c9d2aef65c6b5dca650519a168e3275b2",
+                "79620607484ca1168ae52da7bbf685b100d0e8e9f3444486c3871e963c3a346d",
             "compressed_attention_compress_b300/csrc/block_scan.cuh":
                 "ac0c74255584e15eaea3aa69860c5b08cd4267e432e4e9db82d6c3de8245161a",
         },
