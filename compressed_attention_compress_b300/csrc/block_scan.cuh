@@ -36,4 +36,34 @@ __device__ __forceinline__ int block_exclusive_sum(int v, int *scratch, int &tot
     return scratch[warp] + inc - v;
 }
 
+// Exclusive prefix sums of two values at once (the same barriers as one);
+// `scratch` holds at least 66 ints of shared memory.
+__device__ __forceinline__ int2 block_exclusive_sum2(int a, int b, int *scratch, int &total_a, int &total_b) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int nwarps = (blockDim.x + 31) >> 5;
+    const int ia = warp_inclusive_sum(a), ib = warp_inclusive_sum(b);
+    __syncthreads();  // scratch may still be read by a previous call
+    if (lane == 31) {
+        scratch[warp] = ia;
+        scratch[33 + warp] = ib;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        const int wa = lane < nwarps ? scratch[lane] : 0, wb = lane < nwarps ? scratch[33 + lane] : 0;
+        const int xa = warp_inclusive_sum(wa), xb = warp_inclusive_sum(wb);
+        if (lane < nwarps) {
+            scratch[lane] = xa - wa;
+            scratch[33 + lane] = xb - wb;
+        }
+        if (lane == 31) {
+            scratch[32] = xa;
+            scratch[65] = xb;
+        }
+    }
+    __syncthreads();
+    total_a = scratch[32];
+    total_b = scratch[65];
+    return make_int2(scratch[warp] + ia - a, scratch[33 + warp] + ib - b);
+}
+
 }  // namespace hsa

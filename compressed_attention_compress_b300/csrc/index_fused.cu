@@ -132,7 +132,7 @@ __global__ void __launch_bounds__(kThreads) index_fused_kernel(IndexArgs a, Fuse
     extern __shared__ __align__(16) unsigned char smem[];
     uint32_t *s_keys = reinterpret_cast<uint32_t *>(smem);          // [chunk], kept over all phases
     unsigned *s_h = reinterpret_cast<unsigned *>(smem + (size_t)p.chunk * 4);  // [max(kNB1, nb2)]
-    __shared__ int s_scan[33];
+    __shared__ int s_scan[66];
     __shared__ int s_misc[8];
 
     const int row = blockIdx.y;
@@ -318,7 +318,7 @@ __global__ void __launch_bounds__(kThreads) index_fused_kernel(IndexArgs a, Fuse
     int *s_roff = s_off + (nch + 1);                                 // [nch + 1] offsets past the first spec slots
     const int l_off = (2 * (nch + 1) * 4 + 15) & ~15;
     uint2 *s_l = reinterpret_cast<uint2 *>(smem + p.off_stage_smem + l_off);
-    const int l_cap = (kStages * kStageBytes - l_off) / 8;
+    const int l_cap = (kStages * kStageBytes - l_off) / 8 - 1;  // slot l_cap takes the stores of empty slots
     unsigned *s_h2 = s_h;
     const uint32_t mask2 = (uint32_t)p.nb2 - 1u;
     for (int i = threadIdx.x; i < p.nb2; i += kThreads) s_h2[i] = 0;
@@ -346,8 +346,8 @@ __global__ void __launch_bounds__(kThreads) index_fused_kernel(IndexArgs a, Fuse
                 rest += v > spec ? v - spec : 0;
             }
         int tot, rtot;
-        int o = block_exclusive_sum(loc, s_scan, tot);
-        int ro = block_exclusive_sum(rest, s_scan, rtot);
+        const int2 orr = block_exclusive_sum2(loc, rest, s_scan, tot, rtot);
+        int o = orr.x, ro = orr.y;
         for (int q = 0; q < cpt; ++q)
             if (i0 + q < nch) {
                 const int v = s_off[i0 + q];
@@ -366,18 +366,23 @@ __global__ void __launch_bounds__(kThreads) index_fused_kernel(IndexArgs a, Fuse
     if (total != count_above + n_in && threadIdx.x == 0) raise_flag(FLAG_INDEX_RANGE | 0x400u);
     const bool staged = total <= l_cap;
     const int need = kE - count_above;  // >= 1
+    // a key of b1 is counted in the level-2 histogram (rare: a branch)
+    auto note_b1 = [&](const uint2 &v) {
+        if ((int)(v.x >> p.shift1) == b1) atomicAdd(&s_h2[v.x & mask2], 1u);
+    };
     auto take_in = [&](const uint2 &v, int L) {
         if (staged) s_l[L] = v;
-        if ((int)(v.x >> p.shift1) == b1) atomicAdd(&s_h2[v.x & mask2], 1u);
+        note_b1(v);
     };
 #pragma unroll
     for (int q = 0; q < kSpecPer; ++q) {
         const int sp = q * kThreads + threadIdx.x;
-        const int cc = spec ? sp >> lg_spec : nch;
-        if (cc < nch) {
-            const int i = sp & (spec - 1);
-            if (i < s_off[cc + 1] - s_off[cc]) take_in(sv[q], s_off[cc] + i);
-        }
+        const int cc = spec ? min(sp >> lg_spec, nch) : nch;
+        const int i = sp & (spec - 1);
+        const int lo = s_off[min(cc, nch - 1)], hi = s_off[min(cc, nch - 1) + 1];
+        const bool v = cc < nch && i < hi - lo;
+        if (staged) s_l[v ? lo + i : l_cap] = sv[q];  // empty slots store into the spare slot
+        if (v) note_b1(sv[q]);
     }
     // last c with off[c] <= L (off ascending over [0, nch])
     auto find_chunk = [&](const int *off, int L) {
