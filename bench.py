@@ -709,98 +709,156 @@ def run_hsa(args, ws, rank, local):
 
 def run_e2e(bench, args):
     """Same metric through the Python/C-ABI calls with host buffers: each step copies
-    its inputs (q, indexer query) from pinned host memory, runs the three calls, reads
-    the output back to pinned host memory, and waits for it.  The step's copies and
-    calls are captured once per input replica into a CUDA graph (compression on a
-    second stream beside the indexer, as a serving loop would run them); every step
-    replays one graph and synchronises; the attention's query is copied on the second
-    stream.  `eager_*` is the same step issued call by call on one stream."""
+    its inputs (q, indexer query) from pinned host memory, runs the three calls and
+    copies the output back to pinned host memory, every step inside the timed region.
+
+    `value` pipelines the steps over two input slots and three streams: step i's
+    inputs are copied in on a copy stream as soon as slot i % 2 is free (step i - 2
+    has run), its calls run as one CUDA graph on the compute stream once they have
+    landed, its output is copied out on a third stream behind them, and the host
+    waits for step i - 2's output before it issues step i (two steps in flight, as a
+    serving loop over independent requests would run).  `sync_value` is one graph per
+    step (copies, calls, copy back) replayed and waited for before the next step;
+    `eager_value` the same step issued call by call and waited for."""
     wl = bench.wl
     R = bench.R
+    S = 2  # input slots = steps in flight
     hq = [bench.q[r].cpu().pin_memory() for r in range(R)]
     hqi = [bench.qi[r].cpu().pin_memory() for r in range(R)]
-    hout = torch.empty((wl.B, wl.H, wl.d), dtype=torch.bfloat16).pin_memory()
-    dq = torch.empty_like(bench.q[0])
-    dqi = torch.empty_like(bench.qi[0])
+    hout = [torch.empty((wl.B, wl.H, wl.d), dtype=torch.bfloat16).pin_memory() for _ in range(S)]
+    dq = [torch.empty_like(bench.q[0]) for _ in range(S)]
+    dqi = [torch.empty_like(bench.qi[0]) for _ in range(S)]
     steps = max(20, min(args.steps, 2000))
 
-    def calls(r, side=None):
+    def copies_in(r, s):
+        dq[s].copy_(hq[r], non_blocking=True)
+        dqi[s].copy_(hqi[r], non_blocking=True)
+
+    def compute(r, s, side=None):
+        # inputs already in slot s; the compression runs beside the indexer when a
+        # second stream is given (the one-launch step reads the compressed cache)
         if bench.fused:
-            # the step reads the compressed cache: compress, then the one-launch step; the
-            # query copies travel on the second stream beside the compression
-            if side is None:
-                dq.copy_(hq[r], non_blocking=True)
-                dqi.copy_(hqi[r], non_blocking=True)
-                bench.compress(r)
-            else:
-                fork, join = torch.cuda.Event(), torch.cuda.Event()
-                fork.record()
-                side.wait_event(fork)
-                with torch.cuda.stream(side):
-                    dq.copy_(hq[r], non_blocking=True)
-                    dqi.copy_(hqi[r], non_blocking=True)
-                join.record(side)
-                bench.compress(r)
-                torch.cuda.current_stream().wait_event(join)
-            bench.decode_step(r, qi=dqi, q=dq)
-            hout.copy_(bench.out[r], non_blocking=True)
+            bench.compress(r)
+            bench.decode_step(r, qi=dqi[s], q=dq[s])
             return
         if side is None:
-            dq.copy_(hq[r], non_blocking=True)
-            dqi.copy_(hqi[r], non_blocking=True)
             bench.compress(r)
         else:
-            # the attention's query travels beside the indexer's, with the compression
             fork, join = torch.cuda.Event(), torch.cuda.Event()
             fork.record()
             side.wait_event(fork)
             with torch.cuda.stream(side):
-                dq.copy_(hq[r], non_blocking=True)
                 bench.compress(r)
             join.record(side)
-            dqi.copy_(hqi[r], non_blocking=True)
-        bench.index(r, qi=dqi)
+        bench.index(r, qi=dqi[s])
         if side is not None:
             torch.cuda.current_stream().wait_event(join)
-        bench.attn(r, q=dq)
-        hout.copy_(bench.out[r], non_blocking=True)
+        bench.attn(r, q=dq[s])
 
     def timed(one):
         for i in range(5):
             one(i)
+        torch.cuda.synchronize()
         t = time.perf_counter()
         for i in range(steps):
             one(i)
+        torch.cuda.synchronize()
         return (time.perf_counter() - t) / steps
 
     def eager(i):
-        calls(i % R)
+        r, s = i % R, 0
+        copies_in(r, s)
+        compute(r, s)
+        hout[s].copy_(bench.out[r], non_blocking=True)
         torch.cuda.current_stream().synchronize()
 
     dt_eager = timed(eager)
 
-    graphs = []
     side = torch.cuda.Stream()
     cap = torch.cuda.Stream()
     cap.wait_stream(torch.cuda.current_stream())
+    # one graph per replica of the whole step (copies in, calls, copy out), and one of
+    # the calls alone per (replica, slot)
+    whole, calls_only = [], {}
     for r in range(R):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=cap):
-            calls(r, side)
-        graphs.append(g)
+            copies_in(r, 0)
+            compute(r, 0, side)
+            hout[0].copy_(bench.out[r], non_blocking=True)
+        whole.append(g)
+        for s in range(S):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=cap):
+                compute(r, s, side)
+            calls_only[(r, s)] = g
     torch.cuda.current_stream().wait_stream(cap)
     torch.cuda.synchronize()
 
     def replay(i):
-        graphs[i % R].replay()
+        whole[i % R].replay()
         torch.cuda.current_stream().synchronize()
 
-    dt = timed(replay)
+    dt_sync = timed(replay)
+
+    # Pipelined: graph P[r] runs step r's calls (inputs in slot r % 2) and, beside
+    # them on two more streams, copies step r - 1's output out and step r + 1's
+    # inputs in (R is even, so replica and slot agree step after step).  Graphs run
+    # back to back on one stream; the host waits for graph i - 1 (so for step i - 2's
+    # output) after it launches graph i.  The first step's inputs and the last
+    # step's output are copied outside the graphs, inside the timed region.
+    assert R % S == 0
+    s_a, s_b = torch.cuda.Stream(), torch.cuda.Stream()
+    piped_g = []
+    cap.wait_stream(torch.cuda.current_stream())
+    for r in range(R):
+        g = torch.cuda.CUDAGraph()
+        rp, rn = (r - 1) % R, (r + 1) % R
+        with torch.cuda.graph(g, stream=cap):
+            fork, j1, j2 = torch.cuda.Event(), torch.cuda.Event(), torch.cuda.Event()
+            fork.record()
+            s_a.wait_event(fork)
+            s_b.wait_event(fork)
+            with torch.cuda.stream(s_a):
+                hout[rp % S].copy_(bench.out[rp], non_blocking=True)
+            j1.record(s_a)
+            with torch.cuda.stream(s_b):
+                copies_in(rn, rn % S)
+            j2.record(s_b)
+            compute(r, r % S, side)
+            torch.cuda.current_stream().wait_event(j1)
+            torch.cuda.current_stream().wait_event(j2)
+        piped_g.append(g)
+    torch.cuda.current_stream().wait_stream(cap)
+    torch.cuda.synchronize()
+    done = [torch.cuda.Event() for _ in range(2)]
+
+    def run_piped(n, start):
+        copies_in(start % R, start % S)
+        for i in range(start, start + n):
+            piped_g[i % R].replay()
+            done[i % 2].record()
+            if i > start:
+                done[(i - 1) % 2].synchronize()  # graph i - 1 is done: step i - 2's output is on the host
+        last = (start + n - 1) % R
+        hout[last % S].copy_(bench.out[last], non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+
+    run_piped(8, 0)
+    torch.cuda.synchronize()
+    t = time.perf_counter()
+    run_piped(steps, 0)
+    dt = (time.perf_counter() - t) / steps
+
     h2d = hq[0].numel() * 2 + hqi[0].numel()
-    d2h = hout.numel() * 2
+    d2h = hout[0].numel() * 2
     return {"value": wl.B / dt, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "ms_per_step": dt * 1e3, "steps": steps,
-            "launch": "one CUDA graph per step (replayed, then synchronised)",
+            "launch": "pipelined: one CUDA graph per step runs its calls and, beside them, copies the previous "
+                      "step's output out and the next step's inputs in (2 input slots); graphs back to back on one "
+                      "stream, the host waits for graph i-1 after launching graph i",
+            "sync_value": wl.B / dt_sync, "sync_ms_per_step": dt_sync * 1e3,
+            "sync_launch": "one CUDA graph per step (copies in, calls, copy out), replayed and waited for",
             "eager_value": wl.B / dt_eager, "eager_ms_per_step": dt_eager * 1e3}
 
 
