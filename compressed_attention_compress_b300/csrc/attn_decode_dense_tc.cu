@@ -75,7 +75,7 @@ struct DenseArgs {
     int64_t E_cap, N_cap;
     const int64_t *ctx;  // [B]: the query sits at p = ctx - 1
     float scale_log2;
-    float *part_o;       // [B * HG * t_max][64][128]: unnormalised O of a piece, at the piece's first tile
+    __nv_bfloat16 *part_o;  // [B * HG * t_max][64][128]: unnormalised O of a piece (bf16), at the piece's first tile
     float *part_ml;      // [B * HG * t_max][2][64]: maximum (log2 units), sum
     int *cum;            // [B + 1]: the tile prefix, for the merge
     __nv_bfloat16 *out;  // [B, H, d]
@@ -609,11 +609,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc::tmem_wait_ld();
 #pragma unroll
                 for (int i = 0; i < 2; ++i) {
-                    float *po = a.part_o + (int64_t)slot * (kH * kD) + (int64_t)hh[i] * kD + hf * 64 + 2 * qd;
+                    __nv_bfloat16 *po = a.part_o + (int64_t)slot * (kH * kD) + (int64_t)hh[i] * kD + hf * 64 + 2 * qd;
 #pragma unroll
                     for (int k = 0; k < 8; ++k)
-                        *reinterpret_cast<float2 *>(po + 8 * k) =
-                            make_float2(__uint_as_float(o[4 * k + 2 * i]), __uint_as_float(o[4 * k + 2 * i + 1]));
+                        *reinterpret_cast<uint32_t *>(po + 8 * k) =
+                            pack_bf16x2(__uint_as_float(o[4 * k + 2 * i]), __uint_as_float(o[4 * k + 2 * i + 1]));
                 }
             }
             if (qd == 0) {
@@ -695,50 +695,46 @@ __global__ void __launch_bounds__(kMergeWarps * 32) attn_decode_dense_merge_kern
     __syncthreads();
     const int n = s_n;
     const int hl = blockIdx.y * kMergeWarps + warp;
-    float M = -INFINITY;
-    for (int i = lane; i < n; i += 32) M = fmaxf(M, __ldcg(a.part_ml + (int64_t)s_slot[i] * (2 * kH) + hl));
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    float L = 0.f;
+    // Up to kBatch pieces at a time with every load in flight at once: lane c's
+    // columns 4c..4c+3 of each piece's O, and each piece's maximum and sum (every
+    // lane loads them all; they are one 128-byte line per 32 heads).  The running
+    // maximum M and the sums are rescaled when a later batch raises M.
+    constexpr int kBatch = 16;
+    float M = -INFINITY, L = 0.f;
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    if (M != -INFINITY) {
-        for (int i0 = 0; i0 < n; i0 += 32) {
-            // lane i: weight and sum of piece i0 + i (weight 0: nothing visible there, its O is not read)
-            float w = 0.f, lv = 0.f;
-            if (i0 + lane < n) {
-                const float *pml = a.part_ml + (int64_t)s_slot[i0 + lane] * (2 * kH);
-                const float mv = __ldcg(pml + hl);
-                if (mv != -INFINITY) {
-                    w = tc::ex2(mv - M);
-                    lv = __ldcg(pml + kH + hl);
-                }
-            }
-            const int cnt = n - i0 < 32 ? n - i0 : 32;
-            constexpr int U = 8;
-            for (int k0 = 0; k0 < cnt; k0 += U) {
-                float4 ov[U];
+    for (int i0 = 0; i0 < n; i0 += kBatch) {
+        uint2 ov[kBatch];
+        float mv[kBatch], lv[kBatch];
 #pragma unroll
-                for (int k = 0; k < U; ++k) {
-                    const float wk = __shfl_sync(0xffffffffu, w, (k0 + k) & 31);
-                    ov[k] = (k0 + k < cnt && wk != 0.f)
-                                ? __ldcg(reinterpret_cast<const float4 *>(a.part_o + (int64_t)s_slot[i0 + k0 + k] *
-                                                                                         (kH * kD) +
-                                                                          hl * kD) +
-                                         lane)
-                                : make_float4(0.f, 0.f, 0.f, 0.f);
-                }
+        for (int k = 0; k < kBatch; ++k) {
+            const bool in = i0 + k < n;
+            const int64_t sl = in ? s_slot[i0 + k] : 0;
+            const float *pml = a.part_ml + sl * (2 * kH);
+            mv[k] = in ? __ldcg(pml + hl) : -INFINITY;
+            lv[k] = in ? __ldcg(pml + kH + hl) : 0.f;
+            ov[k] = in ? __ldcg(reinterpret_cast<const uint2 *>(a.part_o + sl * (kH * kD) + (int64_t)hl * kD) + lane)
+                       : make_uint2(0u, 0u);
+        }
+        float bm = -INFINITY;
 #pragma unroll
-                for (int k = 0; k < U; ++k) {
-                    const float wk = __shfl_sync(0xffffffffu, w, (k0 + k) & 31);
-                    const float lk = __shfl_sync(0xffffffffu, lv, (k0 + k) & 31);
-                    if (k0 + k >= cnt || wk == 0.f) continue;
-                    L = fmaf(wk, lk, L);
-                    acc[0] = fmaf(wk, ov[k].x, acc[0]);
-                    acc[1] = fmaf(wk, ov[k].y, acc[1]);
-                    acc[2] = fmaf(wk, ov[k].z, acc[2]);
-                    acc[3] = fmaf(wk, ov[k].w, acc[3]);
-                }
-            }
+        for (int k = 0; k < kBatch; ++k) bm = fmaxf(bm, mv[k]);
+        if (bm == -INFINITY) continue;  // nothing visible in this batch (its O is not used)
+        const float Mn = fmaxf(M, bm);
+        if (M != -INFINITY && Mn != M) {
+            const float r = tc::ex2(M - Mn);
+            L *= r;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[e] *= r;
+        }
+        M = Mn;
+#pragma unroll
+        for (int k = 0; k < kBatch; ++k) {
+            const float wk = mv[k] == -INFINITY ? 0.f : tc::ex2(mv[k] - M);
+            L = fmaf(wk, lv[k], L);
+            acc[0] = fmaf(wk, bf16_lo(ov[k].x), acc[0]);
+            acc[1] = fmaf(wk, bf16_hi(ov[k].x), acc[1]);
+            acc[2] = fmaf(wk, bf16_lo(ov[k].y), acc[2]);
+            acc[3] = fmaf(wk, bf16_hi(ov[k].y), acc[3]);
         }
     }
     const bool empty = !(L > 0.f);
@@ -763,7 +759,7 @@ DecodeDenseWorkspace decode_dense_workspace(int B, int H, int64_t E_cap, int win
     DecodeDenseWorkspace w;
     const size_t slots = (size_t)B * (H / kH) * t_max_of(E_cap, window);  // one per tile of the list, at most
     w.off_o = 0;
-    w.off_ml = (slots * kH * kD * sizeof(float) + 255) & ~(size_t)255;
+    w.off_ml = (slots * kH * kD * sizeof(__nv_bfloat16) + 255) & ~(size_t)255;
     w.off_cum = w.off_ml + ((slots * 2 * kH * sizeof(float) + 255) & ~(size_t)255);
     w.total = w.off_cum + (((size_t)(B + 1) * sizeof(int) + 255) & ~(size_t)255);
     return w;
@@ -806,7 +802,7 @@ cudaError_t launch_attn_decode_dense_tc(const AttnArgs &a, int num_sms, cudaStre
     g.N_cap = a.N_cap;
     g.ctx = a.pos;
     g.scale_log2 = a.scale * kLog2e;
-    g.part_o = a.part_o;
+    g.part_o = reinterpret_cast<__nv_bfloat16 *>(a.part_o);
     g.part_ml = a.part_lse;
     {
         const DecodeDenseWorkspace w = decode_dense_workspace(B, a.H, a.E_cap, a.window);
