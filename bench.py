@@ -1123,6 +1123,8 @@ def parse(argv):
     ap.add_argument("--profile", action="store_true",
                     help="small run for ncu captures: 2 replicas, no end-to-end, CPU or extra legs")
     ap.add_argument("--dry-run", action="store_true", help="launcher self-check on CPU ranks (no GPU work)")
+    ap.add_argument("--only", default=None, choices=sorted(k for k in WORKLOADS if "decode" in k),
+                    help="time only this decode workload (its row alone, for profiling its kernels)")
     args = ap.parse_args(argv)
     args.decode_rows = [r for r in args.decode_rows.split(",") if r]
     if args.profile:
@@ -1143,6 +1145,10 @@ def main(argv=None):
             res = run_dry(args, ws, rank)
         elif args.impl == "reference":
             res = run_reference(args, ws, rank)
+        elif args.only:
+            torch.cuda.set_device(local)
+            row, _ = run_decode(args, ws, rank, local, args.only, args.replicas, fused=False)
+            res = {"only": args.only, "row": row}
         elif args.prefill_only:
             torch.cuda.set_device(local)
             res = {"prefill": run_prefill(torch.device("cuda", local), args.prefill_reps)}
