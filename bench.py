@@ -61,14 +61,14 @@ UNIT = "queries/s"
 # that capture ran (sha256 of each file).
 TRAFFIC = {
     ("index_fused_kernel", "pro_csa_decode"): {
-        "bytes": 67262464 + 526080,
+        "bytes": 67259136 + 525056,
         "sources": {
             "compressed_attention_compress_b300/csrc/index_fused.cu":
-                "22b16b4e825f0b41d03a6b7665f415de88bb1082c1ea4179070ec70817a66404",
+                "12ae7fbe36b53fd0a7d4718beb4249787f0d1a074987417107b5f379e0cadd16",
             "compressed_attention_compress_b300/csrc/common.cuh":
                 "79620607484ca1168ae52da7bbf685b100d0e8e9f3444486c3871e963c3a346d",
             "compressed_attention_compress_b300/csrc/block_scan.cuh":
-                "ac0c74255584e15eaea3aa69860c5b08cd4267e432e4e9db82d6c3de8245161a",
+                "fcbf6072ec91c580a5c6abf47cd7a369531be3b55ac0e10c9af50cbdb7c7dd8d",
         },
     },
 }
