@@ -575,10 +575,12 @@ def time_state_append(bench, steps: int = 64, reps: int = 20) -> float:
                       bench.R, steps, reps)
 
 
-def time_v4_details(bench, steps: int = 64, reps: int = 20) -> dict:
-    """ms per call of the V4-detail kernels a decode step adds around the same attention
-    kernels: RMSNorm + partial RoPE of the step's queries and of each sequence's new
-    entry, and the sink + inverse rotation of the output (CUDA graphs of `steps` calls)."""
+def time_v4_details(bench, steps: int = 64, reps: int = 20):
+    """ms per call of a V4-detail decode step's calls (CUDA graphs of `steps` calls): the
+    attention with the query prep, sink and inverse rotation inside it
+    (hsa_attn_decode_v4), and the RMSNorm + partial RoPE of each sequence's new entry
+    when it is written.  Also, for comparison, the same details as separate passes
+    around the plain attention (query prep, finalize)."""
     wl, L, dev = bench.wl, bench.L, bench.dev
     B, H, d, m = wl.B, wl.H, wl.d, wl.m
     q = bench.q[0].clone()
@@ -591,12 +593,23 @@ def time_v4_details(bench, steps: int = 64, reps: int = 20) -> dict:
     out = bench.out[0].clone()
     lse = torch.zeros((B, H), dtype=torch.float32, device=dev)
     kc = bench.kc[0].clone()
-    calls = {
-        "v4_prep_query": lambda r: L.hsa_rmsnorm_rope(q.view(B, 1, H, d), zeros, ones, 1, pos, 1, 0, gamma),
-        "v4_prep_entry": lambda r: L.hsa_rmsnorm_rope(kc, E_new - 1, E_new, 1, None, m, m - 1, gamma),
-        "v4_finalize": lambda r: L.hsa_attn_finalize(out, lse, pos, sink),
+
+    def attn_v4(r):
+        L.hsa_attn_decode_v4(q, bench.kc[r], bench.kc[r], m, bench.idx[r].view(B, wl.topk), bench.cnt[r].view(B),
+                             bench.k_raw[r], bench.k_raw[r], wl.window, bench.ctx, wl.scale, bench.out[r],
+                             bench.lse[r], bench.ws_a, gamma, 1e-6, 64, 10000.0, sink)
+
+    fused = {
+        "attn_decode_v4": time_graph(attn_v4, bench.R, steps, reps),
+        "v4_prep_entry": time_graph(lambda r: L.hsa_rmsnorm_rope(kc, E_new - 1, E_new, 1, None, m, m - 1, gamma), 1,
+                                    steps, reps),
     }
-    return {name: time_graph(fn, 1, steps, reps) for name, fn in calls.items()}
+    unfused = {
+        "v4_prep_query": time_graph(lambda r: L.hsa_rmsnorm_rope(q.view(B, 1, H, d), zeros, ones, 1, pos, 1, 0, gamma),
+                                    1, steps, reps),
+        "v4_finalize": time_graph(lambda r: L.hsa_attn_finalize(out, lse, pos, sink), 1, steps, reps),
+    }
+    return fused, unfused
 
 
 def decode_row(wl, bench, t, op_ms, ws):
@@ -641,7 +654,8 @@ def run_hsa(args, ws, rank, local):
         head, bench = run_decode(args, ws, rank, local, HEADLINE, args.replicas)
     op_ms = head["op_ms"]
     op_ms["compress_append"] = time_state_append(bench)
-    op_ms.update(time_v4_details(bench))
+    v4_fused, v4_unfused = time_v4_details(bench)
+    op_ms.update(v4_fused)
     op_ms["attn_decode_shared_kv"] = time_graph(lambda r: bench.attn(r, kv_shared=True), bench.R)
     by = algorithmic_bytes(wl, bench.ctx_host.tolist(), bench.cnt_total())
     peak, peak_kind = load_peaks()
@@ -679,6 +693,7 @@ def run_hsa(args, ws, rank, local):
                           "frac": head["step_frac_of_hbm"], "frac_median_of_replays": head["step_frac_of_hbm_median"],
                           "algorithmic_bytes_per_step": by["step"]},
         "op_ms": op_ms,
+        "v4_unfused_ms": v4_unfused,
         "clocks": sampler.summary(),
     }
     del bench

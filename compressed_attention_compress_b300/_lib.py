@@ -23,7 +23,7 @@ _STATUS = {0: "HSA_OK", 1: "HSA_ERR_INVALID_ARG", 2: "HSA_ERR_UNSUPPORTED", 3: "
 
 # every symbol include/hsa.h declares
 EXPORTS = ["hsa_last_error", "hsa_version", "hsa_check", "hsa_check_pointer", "hsa_compress", "hsa_compress_append", "hsa_compress_learned", "hsa_index_topk_workspace_size",
-           "hsa_index_topk", "hsa_index_topk_noalloc", "hsa_attn_decode_workspace_size", "hsa_attn_decode", "hsa_decode_csa_workspace_size", "hsa_decode_csa",
+           "hsa_index_topk", "hsa_index_topk_noalloc", "hsa_attn_decode_workspace_size", "hsa_attn_decode", "hsa_attn_decode_v4", "hsa_decode_csa_workspace_size", "hsa_decode_csa",
            "hsa_attn_prefill_workspace_size", "hsa_attn_prefill", "hsa_index_scores", "hsa_topk_merge",
            "hsa_lse_merge", "hsa_rmsnorm_rope", "hsa_attn_finalize"]
 NOALLOC_SCRATCH_BYTES = 16 << 20
@@ -64,6 +64,9 @@ def _load():
     lib.hsa_attn_decode.restype = I
     lib.hsa_attn_decode.argtypes = [P, I, I, I, I, P, P, I64, I64, I64, I, P, P, I, P, P, I64, I64, I64, I, P, F,
                                     P, P, P, SZ, P]
+    lib.hsa_attn_decode_v4.restype = I
+    # as hsa_attn_decode, with gamma_q, eps, rope_dims, theta and sink before out
+    lib.hsa_attn_decode_v4.argtypes = lib.hsa_attn_decode.argtypes[:22] + [P, F, I, F, P] + lib.hsa_attn_decode.argtypes[22:]
     lib.hsa_decode_csa_workspace_size.restype = I
     lib.hsa_decode_csa_workspace_size.argtypes = [I, I, I, I, I64, ctypes.POINTER(SZ)]
     lib.hsa_decode_csa.restype = I
@@ -192,6 +195,19 @@ def hsa_attn_decode(q, kc, vc, m, idx, cnt, k_raw, v_raw, window, ctx_len, scale
                              int(m), _p(idx), _p(cnt), topk, _p(k_raw), _p(v_raw), k_raw.stride(0), k_raw.stride(1),
                              k_raw.shape[1], int(window), _p(ctx_len), float(scale), _p(out), _p(lse), _p(ws),
                              ws.numel() * ws.element_size() if ws is not None else 0, _stream(stream)))
+
+
+def hsa_attn_decode_v4(q, kc, vc, m, idx, cnt, k_raw, v_raw, window, ctx_len, scale, out, lse=None, ws=None,
+                       gamma_q=None, eps=1e-6, rope_dims=64, theta=10000.0, sink=None, stream=None):
+    """hsa_attn_decode with the V4 query preparation (RMSNorm, partial RoPE) and the sink and
+    inverse rotation of the output inside the attention kernel; q is the raw query."""
+    B, H, d = q.shape
+    topk = idx.shape[-1]
+    _chk(lib.hsa_attn_decode_v4(_p(q), _dt(q), B, H, d, _p(kc), _p(vc), kc.stride(0), kc.stride(1), kc.shape[1],
+                                int(m), _p(idx), _p(cnt), topk, _p(k_raw), _p(v_raw), k_raw.stride(0),
+                                k_raw.stride(1), k_raw.shape[1], int(window), _p(ctx_len), float(scale), _p(gamma_q),
+                                float(eps), int(rope_dims), float(theta), _p(sink), _p(out), _p(lse), _p(ws),
+                                ws.numel() * ws.element_size() if ws is not None else 0, _stream(stream)))
 
 
 def hsa_decode_csa_workspace_size(B, H, d, DI, E_cap):

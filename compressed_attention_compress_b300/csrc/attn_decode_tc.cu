@@ -30,6 +30,8 @@
 // still reaches the cluster barrier and frees its TMEM.
 #include <math.h>
 
+#include <type_traits>
+
 #include "internal.h"
 #include "tc_common.cuh"
 
@@ -65,6 +67,67 @@ struct DecodeTcArgs {
     float *part_o;               // [B, H / 64, n_tiles, 64, d] fp32 partial O
     float *part_ml;              // [B, H / 64, n_tiles, 2, 64]: maximum (log2 units), sum
 };
+// V4 details (the V4 instantiation only): RMSNorm and partial RoPE of the query, sink
+// and inverse rotation of the output
+struct DecodeV4Args {
+    int rope_dims;
+    float eps;
+    const float *gamma_q;        // [d] or null
+    const float *sink;           // [H] or null
+    double inv_freq[kMaxRopeDims / 2];
+};
+struct NoV4Args {};
+
+// cos and sin of pos * inv_freq (inv_freq = theta^(-2k/rope_dims), formed on the host in
+// double): the angle is formed and reduced modulo 2 pi in double precision, then
+// sin/cos are taken in fp32 on the reduced angle (|r| <= pi)
+__device__ __forceinline__ void rope_cs(int64_t pos, double inv_freq, float &c, float &s) {
+    const double ang = (double)pos * inv_freq;
+    const double two_pi = 6.283185307179586476925286766559;
+    const double n = rint(ang * (1.0 / two_pi));
+    const float r = (float)fma(-two_pi, n, ang);
+    sincosf(r, &s, &c);
+}
+
+// Row h of Q (128-byte-swizzled, two 64-column blocks) <- R(p) N(q): RMSNorm with
+// gamma, then channel pair k of the last rope_dims channels turned by the angle
+// (cos, sin)[k] of the query position; one thread per row, in place.
+__device__ __forceinline__ void prep_q_row(unsigned char *sQ, int h, const float *s_g, float eps, int rope_dims,
+                                           const float *s_cs, const float *s_sn, int q_blk) {
+    float ss = 0.f;
+#pragma unroll 4
+    for (int c = 0; c < kD / 8; ++c) {
+        const uint4 u = *reinterpret_cast<const uint4 *>(sQ + (c >> 3) * q_blk + h * 128 + (((c & 7) ^ (h & 7)) << 4));
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float lo = bf16_lo(w[e]), hi = bf16_hi(w[e]);
+            ss = fmaf(lo, lo, fmaf(hi, hi, ss));
+        }
+    }
+    const float inv = 1.f / sqrtf(ss / (float)kD + eps);
+    const int r0 = kD - rope_dims;  // first rotated channel
+#pragma unroll 4
+    for (int c = 0; c < kD / 8; ++c) {
+        unsigned char *ptr = sQ + (c >> 3) * q_blk + h * 128 + (((c & 7) ^ (h & 7)) << 4);
+        const uint4 u = *reinterpret_cast<const uint4 *>(ptr);
+        uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int ch = c * 8 + 2 * e;  // channels ch, ch + 1: one rotation pair when ch >= r0
+            float x0 = bf16_lo(w[e]) * inv * s_g[ch], x1 = bf16_hi(w[e]) * inv * s_g[ch + 1];
+            if (ch >= r0) {
+                const int k = (ch - r0) >> 1;
+                const float cs = s_cs[k], sn = s_sn[k];
+                const float y0 = x0 * cs - x1 * sn;
+                x1 = x0 * sn + x1 * cs;
+                x0 = y0;
+            }
+            w[e] = pack_bf16x2(x0, x1);
+        }
+        *reinterpret_cast<uint4 *>(ptr) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+}
 
 // chunk c (16 bytes) of row r of a 128-byte-swizzled K-major tile made of 64-column blocks
 __device__ __forceinline__ uint32_t sw_off(int r, int c, int blk_bytes) {
@@ -80,7 +143,9 @@ __device__ __forceinline__ bool wait_phase0(uint64_t *bar) {
     return false;
 }
 
-__global__ void __launch_bounds__(kThreads, 1) attn_decode_tc_kernel(DecodeTcArgs a) {
+template <bool V4>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_decode_tc_kernel(DecodeTcArgs a, typename std::conditional<V4, DecodeV4Args, NoV4Args>::type v4) {
     extern __shared__ __align__(16) unsigned char smem_raw[];  // rounded up to 1024 at run time
     unsigned char *smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
     unsigned char *sQ = smem;
@@ -91,6 +156,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_tc_kernel(DecodeTcArg
     __shared__ uint32_t s_mask[kThreads / 32];
     __shared__ __align__(8) uint64_t bar_s, bar_o;
     __shared__ uint32_t s_tmem;
+    // V4: the angles of the query position and gamma_q
+    __shared__ float s_cs[V4 ? kMaxRopeDims / 2 : 1], s_sn[V4 ? kMaxRopeDims / 2 : 1], s_g[V4 ? kD : 1];
 
     const int j = blockIdx.x;  // tile == rank in the cluster
     const int b = blockIdx.y, hg = blockIdx.z;
@@ -164,6 +231,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_tc_kernel(DecodeTcArg
     if (!a.shared_kv) gather(sV, vsrc);
     cp_async_commit();
     const unsigned char *tV = a.shared_kv ? sK : sV;
+    if constexpr (V4) {
+        // R(p) N(q) on Q in shared memory while the K and V rows are in flight
+        if (tid < v4.rope_dims / 2) rope_cs(p, v4.inv_freq[tid], s_cs[tid], s_sn[tid]);
+        for (int i = tid; i < kD; i += kThreads) s_g[i] = v4.gamma_q ? v4.gamma_q[i] : 1.f;
+        cp_async_wait<2>();  // this thread's Q copies (group 0)
+        __syncthreads();     // every thread's, the angles and gamma
+        if (tid < kH) prep_q_row(sQ, tid, s_g, v4.eps, v4.rope_dims, s_cs, s_sn, kQBlk);
+        // (the MMA reads Q through the async proxy: the fence below precedes the barrier)
+    }
 
     // ---- S = Q K^T once Q and every thread's K rows have landed
     cp_async_wait<1>();
@@ -325,15 +401,46 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_tc_kernel(DecodeTcArg
                 acc.w = fmaf(wgt, ov[r].w, acc.w);
             }
         }
-        const bool empty = !(Lsum > 0.f);
-        const float inv = empty ? 0.f : 1.f / Lsum;
         const int hh = hg * kH + hl;
         __nv_bfloat16 *out = a.out + ((int64_t)b * a.H + hh) * kD + c4 * 4;
-        uint2 pk;
-        pk.x = pack_bf16x2(acc.x * inv, acc.y * inv);
-        pk.y = pack_bf16x2(acc.z * inv, acc.w * inv);
-        *reinterpret_cast<uint2 *>(out) = pk;
-        if (a.lse && c4 == 0) a.lse[(int64_t)b * a.H + hh] = empty ? -INFINITY : (M + log2f(Lsum)) * kLn2;
+        if constexpr (!V4) {
+            const bool empty = !(Lsum > 0.f);
+            const float inv = empty ? 0.f : 1.f / Lsum;
+            uint2 pk;
+            pk.x = pack_bf16x2(acc.x * inv, acc.y * inv);
+            pk.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+            *reinterpret_cast<uint2 *>(out) = pk;
+            if (a.lse && c4 == 0) a.lse[(int64_t)b * a.H + hh] = empty ? -INFINITY : (M + log2f(Lsum)) * kLn2;
+        } else {
+            // the sink's logit z joins the denominator (e^z = 2^(z log2 e)), then the
+            // output turns back by the query's position, R(-p)
+            float Mx = M, Lt = Lsum, wa = 1.f;
+            if (v4.sink) {
+                const float zl = v4.sink[hh] * kLog2e;
+                Mx = fmaxf(M, zl);
+                wa = M == -INFINITY ? 0.f : tc::ex2(M - Mx);
+                Lt = Lsum * wa + tc::ex2(zl - Mx);
+            }
+            const bool empty = !(Lt > 0.f);
+            const float inv = empty ? 0.f : wa / Lt;
+            float o4[4] = {acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv};
+#pragma unroll
+            for (int e = 0; e < 4; e += 2) {
+                const int ch = c4 * 4 + e, r0 = kD - v4.rope_dims;
+                if (ch >= r0) {
+                    const int k = (ch - r0) >> 1;
+                    const float cs = s_cs[k], sn = s_sn[k];
+                    const float y0 = o4[e] * cs + o4[e + 1] * sn;
+                    o4[e + 1] = -o4[e] * sn + o4[e + 1] * cs;
+                    o4[e] = y0;
+                }
+            }
+            uint2 pk;
+            pk.x = pack_bf16x2(o4[0], o4[1]);
+            pk.y = pack_bf16x2(o4[2], o4[3]);
+            *reinterpret_cast<uint2 *>(out) = pk;
+            if (a.lse && c4 == 0) a.lse[(int64_t)b * a.H + hh] = empty ? -INFINITY : (Mx + log2f(Lt)) * kLn2;
+        }
     }
     // after a give-up, let this CTA's MMAs finish (again bounded) before TMEM is freed
     if (tid == 0 && !ok) wait_phase0(&bar_s);
@@ -392,19 +499,25 @@ cudaError_t launch_attn_decode_tc(const AttnArgs &a, cudaStream_t s) {
     g.lse = a.lse;
     g.part_o = a.part_o;
     g.part_ml = a.part_lse;
-    static unsigned long long done = 0, np_done = 0;
-    cudaError_t e = smem_limit_once(attn_decode_tc_kernel, (int)kSmemBytes, done);
-    if (e != cudaSuccess) return e;
-    if (g.n_tiles > 8) {
-        int dev = 0;
-        cudaGetDevice(&dev);
-        const unsigned long long bit = 1ull << (dev & 63);
-        if (!(np_done & bit)) {
-            e = cudaFuncSetAttribute(attn_decode_tc_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-            if (e != cudaSuccess) return e;
-            np_done |= bit;
+    static unsigned long long done = 0, np_done = 0, done4 = 0, np_done4 = 0;
+    auto prepare = [&](auto kern, unsigned long long &dn, unsigned long long &npd) {
+        cudaError_t e = smem_limit_once(kern, (int)kSmemBytes, dn);
+        if (e != cudaSuccess) return e;
+        if (g.n_tiles > 8) {
+            int dev = 0;
+            cudaGetDevice(&dev);
+            const unsigned long long bit = 1ull << (dev & 63);
+            if (!(npd & bit)) {
+                e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+                if (e != cudaSuccess) return e;
+                npd |= bit;
+            }
         }
-    }
+        return cudaSuccess;
+    };
+    cudaError_t e = a.v4 ? prepare(attn_decode_tc_kernel<true>, done4, np_done4)
+                         : prepare(attn_decode_tc_kernel<false>, done, np_done);
+    if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(g.n_tiles, a.rows, a.H / kH);
     cfg.blockDim = dim3(kThreads);
@@ -421,7 +534,14 @@ cudaError_t launch_attn_decode_tc(const AttnArgs &a, cudaStream_t s) {
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, attn_decode_tc_kernel, g);
+    if (!a.v4) return cudaLaunchKernelEx(&cfg, attn_decode_tc_kernel<false>, g, NoV4Args{});
+    DecodeV4Args v;
+    v.rope_dims = a.rope_dims;
+    v.eps = a.eps;
+    v.gamma_q = a.gamma_q;
+    v.sink = a.sink;
+    for (int k = 0; k < kMaxRopeDims / 2; ++k) v.inv_freq[k] = a.inv_freq[k];
+    return cudaLaunchKernelEx(&cfg, attn_decode_tc_kernel<true>, g, v);
 }
 
 }  // namespace hsa

@@ -484,6 +484,54 @@ hsa_status_t hsa_attn_decode(const void *q, hsa_dtype_t dt, int B, int H, int d,
     return launched(hsa::launch_attn_merge(a, dt == HSA_BF16, s), "attn_merge");
 }
 
+hsa_status_t hsa_attn_decode_v4(const void *q, hsa_dtype_t dt, int B, int H, int d, const void *kc, const void *vc,
+                                int64_t c_sb, int64_t c_se, int64_t E_cap, int m, const int32_t *idx,
+                                const int32_t *cnt, int topk, const void *k_raw, const void *v_raw, int64_t r_sb,
+                                int64_t r_st, int64_t N_cap, int window, const int64_t *ctx_len, float scale,
+                                const float *gamma_q, float eps, int rope_dims, float theta, const float *sink,
+                                void *out, float *lse, void *ws, size_t ws_bytes, hsa_stream_t stream) {
+    hsa_status_t st = check_attn_common(q, dt, B, 1, H, d, kc, vc, c_sb, c_se, E_cap, m, idx, topk, k_raw, v_raw,
+                                        r_sb, r_st, N_cap, window, ctx_len, out);
+    if (st != HSA_OK) return st;
+    if (rope_dims < 0 || rope_dims % 2 || rope_dims > d || !(theta > 0.f) || !(eps >= 0.f))
+        return fail(HSA_ERR_INVALID_ARG, "rope_dims must be even in [0, d]; theta > 0, eps >= 0");
+    if (B == 0) return ok();
+    if (dt != HSA_BF16 || d != 128 || !idx || !hsa::decode_tc_shape(H, d, topk, window))
+        return fail(HSA_ERR_UNSUPPORTED,
+                    "hsa_attn_decode_v4 runs on the tensor-core CSA decode path: bf16, d = 128, H a multiple of 64, "
+                    "selected entries (idx), topk + window <= 2048");
+    DevInfo di;
+    if ((st = device_info(di)) != HSA_OK) return st;
+    const DecodePlan p = plan_decode(dt, B, H, d, E_cap, m, topk, window, false, di.num_sms);
+    if (p.total > 0 && (!ws || ws_bytes < p.total))
+        return fail(HSA_ERR_WORKSPACE, "decode workspace needs %zu bytes, got %zu", p.total, ws_bytes);
+    if (p.total > 0 && (reinterpret_cast<uintptr_t>(ws) & 255) != 0)
+        return fail(HSA_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+    if ((st = check_pointers({{cnt, "cnt"}, {lse, "lse"}, {p.total > 0 ? ws : nullptr, "workspace"},
+                              {gamma_q, "gamma_q"}, {sink, "sink"}})) != HSA_OK)
+        return st;
+    if ((st = pending_error()) != HSA_OK) return st;
+    hsa::AttnArgs a{};
+    a.q = q; a.rows = B; a.T = 1; a.H = H; a.d = d;
+    a.kc = kc; a.vc = vc; a.c_sb = c_sb; a.c_se = c_se; a.E_cap = E_cap; a.m = m;
+    a.idx = idx; a.cnt = cnt; a.topk = topk;
+    a.k_raw = k_raw; a.v_raw = v_raw; a.r_sb = r_sb; a.r_st = r_st; a.N_cap = N_cap; a.window = window;
+    a.pos = ctx_len; a.pos_is_ctx = 1; a.scale = scale; a.out = out; a.lse = lse;
+    a.shared_kv = kc == vc && k_raw == v_raw;
+    a.split = p.split; a.max_splits = p.max_splits;
+    a.part_o = p.total ? reinterpret_cast<float *>(static_cast<char *>(ws) + p.off_o) : nullptr;
+    a.part_lse = p.total ? reinterpret_cast<float *>(static_cast<char *>(ws) + p.off_lse) : nullptr;
+    a.v4 = 1;
+    a.gamma_q = gamma_q;
+    a.sink = sink;
+    a.eps = eps;
+    a.rope_dims = rope_dims;
+    for (int k = 0; k < rope_dims / 2; ++k) a.inv_freq[k] = pow((double)theta, -2.0 * k / rope_dims);
+    if (p.split >= 0 || !hsa::decode_tc_supported(a))
+        return fail(HSA_ERR_UNSUPPORTED, "hsa_attn_decode_v4: this shape does not take the tensor-core decode path");
+    return launched(hsa::launch_attn_decode_tc(a, reinterpret_cast<cudaStream_t>(stream)), "attn_decode_v4");
+}
+
 hsa_status_t hsa_decode_csa_workspace_size(int B, int H, int d, int DI, int64_t E_cap, size_t *bytes) {
     if (!bytes) return fail(HSA_ERR_INVALID_ARG, "null bytes");
     if (B < 0 || H <= 0 || d <= 0 || DI <= 0 || E_cap < 0) return fail(HSA_ERR_INVALID_ARG, "bad size");

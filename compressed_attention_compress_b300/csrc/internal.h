@@ -199,6 +199,15 @@ struct AttnArgs {
     int max_splits;
     float *part_o;      // [rows, max_splits, H, d]
     float *part_lse;    // [rows, max_splits, H]
+    // V4 details fused into the tcgen05 CSA decode attention (v4 != 0): RMSNorm
+    // (gamma_q) and partial RoPE of the query in shared memory, attention sink and
+    // inverse rotation of the output in the merge
+    int v4;
+    const float *gamma_q;  // [d] or null (ones)
+    const float *sink;     // [H] or null (no sink)
+    float eps;
+    int rope_dims;
+    double inv_freq[kMaxRopeDims / 2];
 };
 int attn_split_size(bool bf16, bool dense, int H, int rows, int64_t max_items, int num_sms);
 cudaError_t launch_attn_bf16(const AttnArgs &a, cudaStream_t s);

@@ -368,6 +368,35 @@ HSA_API hsa_status_t hsa_attn_prefill(const void *q, hsa_dtype_t dt, int B, int 
  *   out        [B, T, H, d] of `dt`, contiguous;  lse fp32 [B, T, H]
  *   sink       device fp32 [H] or NULL (no sink: lse unchanged)
  */
+/*
+ * hsa_attn_decode_v4 -- the same V4 decode attention with the query's
+ * preparation and the finalization inside the attention kernel (QbitAI
+ * article, 混合注意力机制, the Q/KV normalisation, partial RoPE, shared
+ * key/value and attention-sink paragraphs): q is the raw query; the kernel
+ * forms R(p) N_q(q) in shared memory (N_q with gamma_q and eps, R turning the
+ * last rope_dims channels by p * theta^(-2k / rope_dims), p = ctx_len - 1),
+ * attends to the selected entries and the window exactly as hsa_attn_decode,
+ * and writes out = R(-p) sum_x softmax'(logit)_x v_x and lse = ln(sum_x
+ * e^logit_x + e^sink[h]) -- the result of hsa_rmsnorm_rope on q, then
+ * hsa_attn_decode, then hsa_attn_finalize, in one launch.  The entries and
+ * window tokens must already be prepared (hsa_rmsnorm_rope when they are
+ * written).  Arguments as hsa_attn_decode (workspace of
+ * hsa_attn_decode_workspace_size bytes), plus:
+ *   gamma_q    device fp32 [d] or NULL (ones);  eps >= 0
+ *   rope_dims  even, 0 <= rope_dims <= d;  theta > 0
+ *   sink       device fp32 [H] or NULL (no sink)
+ * Runs on the tensor-core CSA decode path only: bf16, d = 128, H a multiple of
+ * 64, idx non-NULL, topk + window <= 2048; other shapes return
+ * HSA_ERR_UNSUPPORTED.  q is not modified.
+ */
+HSA_API hsa_status_t hsa_attn_decode_v4(const void *q, hsa_dtype_t dt, int B, int H, int d, const void *kc,
+                                        const void *vc, int64_t c_sb, int64_t c_se, int64_t E_cap, int m,
+                                        const int32_t *idx, const int32_t *cnt, int topk, const void *k_raw,
+                                        const void *v_raw, int64_t r_sb, int64_t r_st, int64_t N_cap, int window,
+                                        const int64_t *ctx_len, float scale, const float *gamma_q, float eps,
+                                        int rope_dims, float theta, const float *sink, void *out, float *lse,
+                                        void *ws, size_t ws_bytes, hsa_stream_t stream);
+
 HSA_API hsa_status_t hsa_rmsnorm_rope(void *x, hsa_dtype_t dt, int B, int H, int d, int64_t x_sb, int64_t x_sn,
                                       int64_t n_cap, const int64_t *n_begin, const int64_t *n_end,
                                       int64_t max_rows, const int64_t *pos_base, int64_t pos_stride,

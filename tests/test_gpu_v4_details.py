@@ -40,10 +40,13 @@ def _inputs(seed, B, E_cap, N, H, d):
     return ent, raw, gq, gk, sink, g
 
 
-@pytest.mark.parametrize("use_sink", [True, False])
-def test_v4_decode_csa(lib, use_sink):
+@pytest.mark.parametrize("use_sink,fused,H", [(True, False, 64), (False, False, 64), (True, True, 64),
+                                               (False, True, 64), (True, True, 128)])
+def test_v4_decode_csa(lib, use_sink, fused, H):
+    """fused: the raw query into hsa_attn_decode_v4 (query prep, sink and inverse rotation
+    inside the attention kernel); else hsa_rmsnorm_rope, hsa_attn_decode, hsa_attn_finalize"""
     dev = torch.device("cuda")
-    B, H, d, m, W, topk = 2, 64, 128, 4, 128, 256
+    B, d, m, W, topk = 2, 128, 4, 128, 256
     E_cap = 2048
     N = E_cap * m
     ent, raw, gq, gk, sink, g = _inputs(31, B, E_cap, N, H, d)
@@ -56,16 +59,22 @@ def test_v4_decode_csa(lib, use_sink):
     scale = 1.0 / d ** 0.5
     qd, entd, rawd = q.to(dev), ent.to(dev), raw.to(dev)
     gqd, gkd = gq.to(dev), gk.to(dev)
-    _prep(lib, qd.view(B, 1, H, d), [0] * B, [1] * B, 1, ctx - 1, 1, 0, gqd)
+    if not fused:
+        _prep(lib, qd.view(B, 1, H, d), [0] * B, [1] * B, 1, ctx - 1, 1, 0, gqd)
     _prep(lib, entd, [0] * B, E.tolist(), E_cap, None, m, m - 1, gkd)
     _prep(lib, rawd, np.maximum(ctx - W, 0).tolist(), ctx.tolist(), W, None, 1, 0, gkd)
     out = torch.empty((B, H, d), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((B, H), dtype=torch.float32, device=dev)
     ws = lib.workspace(lib.hsa_attn_decode_workspace_size(torch.bfloat16, B, H, d, E_cap, m, topk, W))
     ctxd = torch.as_tensor(ctx, dtype=torch.int64, device=dev)
-    lib.hsa_attn_decode(qd, entd, entd, m, torch.from_numpy(idx).to(dev), None, rawd, rawd, W, ctxd, scale, out, lse,
-                        ws)
-    lib.hsa_attn_finalize(out, lse, ctxd - 1, sink.to(dev) if use_sink else None, RD, THETA)
+    if fused:
+        lib.hsa_attn_decode_v4(qd, entd, entd, m, torch.from_numpy(idx).to(dev), None, rawd, rawd, W, ctxd, scale, out,
+                               lse, ws, gqd, EPS, RD, THETA, sink.to(dev) if use_sink else None)
+        assert torch.equal(qd.cpu(), q)  # the raw query is left as it was
+    else:
+        lib.hsa_attn_decode(qd, entd, entd, m, torch.from_numpy(idx).to(dev), None, rawd, rawd, W, ctxd, scale, out,
+                            lse, ws)
+        lib.hsa_attn_finalize(out, lse, ctxd - 1, sink.to(dev) if use_sink else None, RD, THETA)
     lib.hsa_check()
     ro, rl = oracle.attn_v4_rows(host_np(q), np.arange(B), ctx - 1, host_np(ent), m, idx, host_np(raw), W, scale,
                                  gq.double().numpy(), gk.double().numpy(), EPS, RD, THETA,
