@@ -578,9 +578,9 @@ def time_state_append(bench, steps: int = 64, reps: int = 20) -> float:
 def time_v4_details(bench, steps: int = 64, reps: int = 20):
     """ms per call of a V4-detail decode step's calls (CUDA graphs of `steps` calls): the
     attention with the query prep, sink and inverse rotation inside it
-    (hsa_attn_decode_v4), and the RMSNorm + partial RoPE of each sequence's new entry
-    when it is written.  Also, for comparison, the same details as separate passes
-    around the plain attention (query prep, finalize)."""
+    (hsa_attn_decode_v4), and the new block's compression with the entry's RMSNorm +
+    partial RoPE as it is written (hsa_compress_v4).  Also, for comparison, the same
+    details as separate passes around the plain calls (query prep, entry prep, finalize)."""
     wl, L, dev = bench.wl, bench.L, bench.dev
     B, H, d, m = wl.B, wl.H, wl.d, wl.m
     q = bench.q[0].clone()
@@ -601,12 +601,14 @@ def time_v4_details(bench, steps: int = 64, reps: int = 20):
 
     fused = {
         "attn_decode_v4": time_graph(attn_v4, bench.R, steps, reps),
-        "v4_prep_entry": time_graph(lambda r: L.hsa_rmsnorm_rope(kc, E_new - 1, E_new, 1, None, m, m - 1, gamma), 1,
-                                    steps, reps),
+        "compress_v4": time_graph(lambda r: L.hsa_compress_v4(bench.k_raw[r], bench.tb, bench.te, 1, bench.w, m, kc,
+                                                              gamma), bench.R, steps, reps),
     }
     unfused = {
         "v4_prep_query": time_graph(lambda r: L.hsa_rmsnorm_rope(q.view(B, 1, H, d), zeros, ones, 1, pos, 1, 0, gamma),
                                     1, steps, reps),
+        "v4_prep_entry": time_graph(lambda r: L.hsa_rmsnorm_rope(kc, E_new - 1, E_new, 1, None, m, m - 1, gamma), 1,
+                                    steps, reps),
         "v4_finalize": time_graph(lambda r: L.hsa_attn_finalize(out, lse, pos, sink), 1, steps, reps),
     }
     return fused, unfused

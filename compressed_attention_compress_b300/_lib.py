@@ -22,7 +22,7 @@ _STATUS = {0: "HSA_OK", 1: "HSA_ERR_INVALID_ARG", 2: "HSA_ERR_UNSUPPORTED", 3: "
            4: "HSA_ERR_CUDA", 5: "HSA_ERR_DEVICE_FLAG"}
 
 # every symbol include/hsa.h declares
-EXPORTS = ["hsa_last_error", "hsa_version", "hsa_check", "hsa_check_pointer", "hsa_compress", "hsa_compress_append", "hsa_compress_learned", "hsa_index_topk_workspace_size",
+EXPORTS = ["hsa_last_error", "hsa_version", "hsa_check", "hsa_check_pointer", "hsa_compress", "hsa_compress_v4", "hsa_compress_append", "hsa_compress_learned", "hsa_index_topk_workspace_size",
            "hsa_index_topk", "hsa_index_topk_noalloc", "hsa_attn_decode_workspace_size", "hsa_attn_decode", "hsa_attn_decode_v4", "hsa_decode_csa_workspace_size", "hsa_decode_csa",
            "hsa_attn_prefill_workspace_size", "hsa_attn_prefill", "hsa_index_scores", "hsa_topk_merge",
            "hsa_lse_merge", "hsa_rmsnorm_rope", "hsa_attn_finalize"]
@@ -49,6 +49,8 @@ def _load():
     lib.hsa_check_pointer.argtypes = [P]
     lib.hsa_compress.restype = I
     lib.hsa_compress.argtypes = [P, P, I, I, I, I64, I64, I64, P, P, I64, P, I, P, P, I64, I64, I64, P]
+    lib.hsa_compress_v4.restype = I
+    lib.hsa_compress_v4.argtypes = [P, I, I, I, I64, I64, I64, P, P, I64, P, I, P, I64, I64, I64, P, F, I, F, P]
     lib.hsa_compress_learned.restype = I
     lib.hsa_compress_learned.argtypes = [P, P, I, I, I, I64, I64, I64, P, P, I64, P, P, I, I, P, P, I64, I64, I64, P]
     lib.hsa_compress_append.restype = I
@@ -123,6 +125,16 @@ def hsa_check(stream=None):
 def hsa_check_pointer(ptr: int):
     """Raise HSAError unless the address `ptr` is device memory of the current device (or managed)."""
     _chk(lib.hsa_check_pointer(ctypes.c_void_p(ptr)))
+
+
+def hsa_compress_v4(k, tok_begin, tok_end, max_blocks, w, m, kc, gamma=None, eps=1e-6, rope_dims=64, theta=10000.0,
+                    stream=None):
+    """k [B, N_cap, d] -> kc [B, E_cap, d]: compressed V4 entries (one entry is key and value),
+    normalised with gamma and rotated to their block's last token as they are written."""
+    B, N_cap, d = k.shape
+    _chk(lib.hsa_compress_v4(_p(k), _dt(k), B, d, k.stride(0), k.stride(1), N_cap, _p(tok_begin), _p(tok_end),
+                             int(max_blocks), _p(w), int(m), _p(kc), kc.stride(0), kc.stride(1), kc.shape[1],
+                             _p(gamma), float(eps), int(rope_dims), float(theta), _stream(stream)))
 
 
 def hsa_compress(k, v, tok_begin, tok_end, max_blocks, w, m, kc, vc, stream=None):

@@ -96,6 +96,74 @@ __global__ void __launch_bounds__(256) compress_kernel(CompressArgs a) {
     }
 }
 
+// V4 entries (one tensor; the entry is both key and value): one warp per entry, lane l
+// owns channels [l * d/32, (l+1) * d/32).  The weighted sum runs in fp32 in the order
+// r = 0..m-1; then RMSNorm over the row (gamma, eps) and the rotation of channel pair
+// k of the last rope_dims channels by ((j+1)m - 1) * theta^(-2k/rope_dims) (angle
+// formed and reduced in double), rounded once to the storage type.
+template <typename T>
+__global__ void __launch_bounds__(128) compress_v4_kernel(CompressArgs a, CompressV4Args v) {
+    const int b = blockIdx.y;
+    const int lane = threadIdx.x & 31;
+    const int64_t j0 = a.tok_begin[b] / a.m, j1 = a.tok_end[b] / a.m;
+    const int64_t j = j0 + (int64_t)blockIdx.x * 4 + (threadIdx.x >> 5);
+    if (j >= j1) return;
+    if (a.tok_begin[b] < 0 || (j + 1) * a.m > a.N_cap || j >= a.E_cap) {
+        if (lane == 0) raise_flag(FLAG_COMPRESS_RANGE);
+        return;
+    }
+    const int per = a.d / 32;  // even, <= 16
+    const int c0 = lane * per;
+    const T *x = static_cast<const T *>(a.k) + b * a.in_sb + j * a.m * a.in_st + c0;
+    float acc[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e) acc[e] = 0.f;
+    for (int r = 0; r < a.m; ++r) {
+        const float wr = a.w[r];
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+            if (e < per) acc[e] = fmaf(wr, load_elem(x + (int64_t)r * a.in_st + e), acc[e]);
+    }
+    float ss = 0.f;
+#pragma unroll
+    for (int e = 0; e < 16; ++e)
+        if (e < per) ss = fmaf(acc[e], acc[e], ss);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    const float inv = 1.f / sqrtf(ss / (float)a.d + v.eps);
+    const int64_t pos = (j + 1) * a.m - 1;
+    T *out = static_cast<T *>(a.kc) + b * a.out_sb + j * a.out_se + c0;
+#pragma unroll
+    for (int e = 0; e < 16; e += 2) {
+        if (e >= per) break;
+        const int c = c0 + e;
+        float x0 = acc[e] * inv * (v.gamma ? v.gamma[c] : 1.f);
+        float x1 = acc[e + 1] * inv * (v.gamma ? v.gamma[c + 1] : 1.f);
+        if (c >= a.d - v.rope_dims) {
+            const double ang = (double)pos * v.inv_freq[(c - (a.d - v.rope_dims)) >> 1];
+            const double two_pi = 6.283185307179586476925286766559;
+            const float rr = (float)fma(-two_pi, rint(ang * (1.0 / two_pi)), ang);
+            float sn, cs;
+            sincosf(rr, &sn, &cs);
+            const float y0 = x0 * cs - x1 * sn;
+            x1 = x0 * sn + x1 * cs;
+            x0 = y0;
+        }
+        store_elem(out + e, x0);
+        store_elem(out + e + 1, x1);
+    }
+}
+
+cudaError_t launch_compress_v4(const CompressArgs &a, const CompressV4Args &v, bool bf16, cudaStream_t s) {
+    if (a.B <= 0 || a.max_blocks <= 0) return cudaSuccess;
+    dim3 grid((unsigned)((a.max_blocks + 3) / 4), a.B);
+    if (bf16)
+        compress_v4_kernel<__nv_bfloat16><<<grid, 128, 0, s>>>(a, v);
+    else
+        compress_v4_kernel<float><<<grid, 128, 0, s>>>(a, v);
+    return cudaGetLastError();
+}
+
 // Few long blocks (HCA, m = 128, one block per sequence in a decode step): one CTA
 // per (block, sequence, K or V) copies the block's m rows into shared memory with
 // every 16-byte load in flight at once, then each thread folds its channels over

@@ -268,6 +268,36 @@ hsa_status_t hsa_compress(const void *k, const void *v, hsa_dtype_t dt, int B, i
                     "compress");
 }
 
+hsa_status_t hsa_compress_v4(const void *k, hsa_dtype_t dt, int B, int d, int64_t in_sb, int64_t in_st,
+                             int64_t N_cap, const int64_t *tok_begin, const int64_t *tok_end, int64_t max_blocks,
+                             const float *w, int m, void *kc, int64_t out_sb, int64_t out_se, int64_t E_cap,
+                             const float *gamma, float eps, int rope_dims, float theta, hsa_stream_t stream) {
+    if (!dtype_ok(dt)) return fail(HSA_ERR_UNSUPPORTED, "dtype %d", (int)dt);
+    if (B < 0 || d <= 0 || m <= 0 || max_blocks < 0 || N_cap < 0 || E_cap < 0)
+        return fail(HSA_ERR_INVALID_ARG, "bad size (B=%d d=%d m=%d max_blocks=%lld)", B, d, m, (long long)max_blocks);
+    if (m > 4096) return fail(HSA_ERR_UNSUPPORTED, "m > 4096");
+    if (d % 64 || d > 512) return fail(HSA_ERR_UNSUPPORTED, "d must be a multiple of 64 up to 512, got %d", d);
+    if (rope_dims < 0 || rope_dims % 2 || rope_dims > d || !(theta > 0.f) || !(eps >= 0.f))
+        return fail(HSA_ERR_INVALID_ARG, "rope_dims must be even in [0, d]; theta > 0, eps >= 0");
+    if (rope_dims > hsa::kMaxRopeDims) return fail(HSA_ERR_UNSUPPORTED, "rope_dims above %d", hsa::kMaxRopeDims);
+    if (B > 65535) return fail(HSA_ERR_UNSUPPORTED, "B above 65535");
+    if (B == 0 || max_blocks == 0) return ok();
+    if (!k || !kc || !tok_begin || !tok_end || !w) return fail(HSA_ERR_INVALID_ARG, "null pointer");
+    if (in_st < d || out_se < d) return fail(HSA_ERR_INVALID_ARG, "row strides overlap rows");
+    DevInfo di;
+    hsa_status_t st = device_info(di);
+    if (st != HSA_OK) return st;
+    if ((st = check_pointers({{k, "k"}, {tok_begin, "tok_begin"}, {tok_end, "tok_end"}, {w, "w"}, {kc, "kc"},
+                              {gamma, "gamma"}})) != HSA_OK)
+        return st;
+    if ((st = pending_error()) != HSA_OK) return st;
+    hsa::CompressArgs a{k, k, B, d, in_sb, in_st, N_cap, tok_begin, tok_end, max_blocks, w, m, kc, kc, out_sb, out_se, E_cap};
+    hsa::CompressV4Args v{gamma, eps, rope_dims, {}};
+    for (int i = 0; i < rope_dims / 2; ++i) v.inv_freq[i] = pow((double)theta, -2.0 * i / rope_dims);
+    return launched(hsa::launch_compress_v4(a, v, dt == HSA_BF16, reinterpret_cast<cudaStream_t>(stream)),
+                    "compress_v4");
+}
+
 hsa_status_t hsa_compress_learned(const void *k, const void *v, hsa_dtype_t dt, int B, int d, int64_t in_sb,
                                   int64_t in_st, int64_t N_cap, const int64_t *tok_begin, const int64_t *tok_end,
                                   int64_t max_blocks, const float *u, const float *bias, int m, int L, void *kc,

@@ -19,6 +19,15 @@ struct CompressArgs {
     int64_t out_sb, out_se, E_cap;
 };
 cudaError_t launch_compress(const CompressArgs &a, bool bf16, int num_sms, cudaStream_t s);
+// V4: the entries of one tensor (one entry is both key and value) normalised with
+// gamma (RMSNorm) and turned by R((j+1)m - 1) as they are written.
+struct CompressV4Args {
+    const float *gamma;  // [d] or null (ones)
+    float eps;
+    int rope_dims;
+    double inv_freq[64];
+};
+cudaError_t launch_compress_v4(const CompressArgs &a, const CompressV4Args &v, bool bf16, cudaStream_t s);
 struct CompressAppendArgs {
     const void *k_new, *v_new;  // [B, T, d]
     int B, T, d;

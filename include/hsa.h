@@ -119,6 +119,26 @@ HSA_API hsa_status_t hsa_compress(const void *k, const void *v, hsa_dtype_t dt, 
                           hsa_stream_t stream);
 
 /*
+ * hsa_compress_v4 -- hsa_compress for V4's shared key/value entries, with the
+ * entry's preparation as it is written (QbitAI article, 混合注意力机制: the
+ * KV normalisation and partial RoPE paragraphs; one entry serves as key and
+ * value):  kc[b, j] = R((j+1)m - 1) N(sum_{r<m} w[r] k[b, j*m + r])
+ * with N RMSNorm (gamma, eps) and R the rotation of the last rope_dims
+ * channels as in hsa_rmsnorm_rope; the sum runs in fp32 in the order
+ * r = 0..m-1 and the result is rounded once to `dt`.  Arguments as
+ * hsa_compress for the one tensor k -> kc, plus gamma (device fp32 [d] or
+ * NULL), eps >= 0, rope_dims (even, <= min(d, 128)) and theta > 0.
+ * d a multiple of 64, d <= 512.  The result equals hsa_compress followed by
+ * hsa_rmsnorm_rope on the new entries up to that call's rounding of the
+ * intermediate entry.
+ */
+HSA_API hsa_status_t hsa_compress_v4(const void *k, hsa_dtype_t dt, int B, int d, int64_t in_sb, int64_t in_st,
+                                     int64_t N_cap, const int64_t *tok_begin, const int64_t *tok_end,
+                                     int64_t max_blocks, const float *w, int m, void *kc, int64_t out_sb,
+                                     int64_t out_se, int64_t E_cap, const float *gamma, float eps, int rope_dims,
+                                     float theta, hsa_stream_t stream);
+
+/*
  * hsa_compress_learned -- attention-like compression with learned weights
  * (QbitAI article, 混合注意力机制: CSA step 1 merges every m tokens "through an
  * attention-like mechanism with learned weights"; the HCA paragraph: m' = 128
@@ -342,6 +362,9 @@ HSA_API hsa_status_t hsa_attn_prefill(const void *q, hsa_dtype_t dt, int B, int 
  * the query, the compressed entries and the raw window tokens with
  * hsa_rmsnorm_rope, pass one buffer as both kc and vc (and as both k_raw and
  * v_raw), request lse from the attention call, then apply hsa_attn_finalize.
+ * For CSA decode, hsa_compress_v4 prepares each entry as it is written and
+ * hsa_attn_decode_v4 takes the raw query and applies the sink and the inverse
+ * rotation itself (below), so only the window tokens need hsa_rmsnorm_rope.
  * The result is
  *   q~ = R(p) N_q(q),  e~_x = R(t_x) N_kv(e_x),  logit_x = scale <q~, e~_x>,
  *   out = R(-p) sum_x softmax'(logit)_x e~_x,  lse = ln(sum_x e^logit_x + e^z_h)

@@ -137,3 +137,51 @@ def test_rmsnorm_rope_matches_definition(lib):
                 v[d - RD::2], v[d - RD + 1::2] = z.real, z.imag
                 want[b, r, h] = v
     np.testing.assert_allclose(got, want, atol=2e-5, rtol=1e-5)
+
+
+def test_v4_decode_from_raw_tokens(lib):
+    """the V4 decode path with each preparation inside a kernel that writes or reads the
+    vectors: entries compressed and prepared as they are written (hsa_compress_v4), the raw
+    query into hsa_attn_decode_v4 (query prep, sink, inverse rotation inside), window tokens
+    prepared when they are written -- against the oracle on the raw tokens"""
+    dev = torch.device("cuda")
+    B, H, d, m, W, topk = 2, 128, 128, 4, 128, 256
+    E_cap = 2048
+    N = E_cap * m
+    _, raw, gq, gk, sink, g = _inputs(33, B, E_cap, N, H, d)
+    w = torch.rand((m,), generator=g, dtype=torch.float64) + 0.1
+    w = (w / w.sum()).float()
+    q = torch.randn((B, H, d), generator=g).to(torch.bfloat16)
+    ctx = np.array([N, 5001])
+    E = ctx // m
+    idx = np.full((B, topk), -1, np.int32)
+    for b in range(B):
+        idx[b] = np.sort(np.random.default_rng(40 + b).choice(E[b], topk, replace=False))
+    scale = 1.0 / d ** 0.5
+    rawd = raw.to(dev)
+    gqd, gkd, wd = gq.to(dev), gk.to(dev), w.to(dev)
+    tb = torch.zeros(B, dtype=torch.int64, device=dev)
+    te = torch.as_tensor(ctx, dtype=torch.int64, device=dev)
+    kc = torch.zeros((B, E_cap, d), dtype=torch.bfloat16, device=dev)
+    lib.hsa_compress_v4(rawd, tb, te, E_cap, wd, m, kc, gkd, EPS, RD, THETA)
+    # the same entries by hsa_compress, then hsa_rmsnorm_rope: equal up to the rounding
+    # of the intermediate entry
+    kc2 = torch.zeros_like(kc)
+    lib.hsa_compress(rawd, rawd, tb, te, E_cap, wd, m, kc2, kc2.clone())
+    _prep(lib, kc2, [0] * B, E.tolist(), E_cap, None, m, m - 1, gkd)
+    torch.testing.assert_close(kc.float(), kc2.float(), rtol=2 ** -6, atol=2e-2)
+    rawp = rawd.clone()
+    _prep(lib, rawp, np.maximum(ctx - W, 0).tolist(), ctx.tolist(), W, None, 1, 0, gkd)
+    qd = q.to(dev)
+    out = torch.empty((B, H, d), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((B, H), dtype=torch.float32, device=dev)
+    ws = lib.workspace(lib.hsa_attn_decode_workspace_size(torch.bfloat16, B, H, d, E_cap, m, topk, W))
+    ctxd = torch.as_tensor(ctx, dtype=torch.int64, device=dev)
+    lib.hsa_attn_decode_v4(qd, kc, kc, m, torch.from_numpy(idx).to(dev), None, rawp, rawp, W, ctxd, scale, out, lse,
+                           ws, gqd, EPS, RD, THETA, sink.to(dev))
+    lib.hsa_check()
+    ent = oracle.compress(host_np(raw), w.numpy(), m, [0] * B, ctx.tolist(), E_cap)
+    ro, rl = oracle.attn_v4_rows(host_np(q), np.arange(B), ctx - 1, ent, m, idx, host_np(raw), W, scale,
+                                 gq.double().numpy(), gk.double().numpy(), EPS, RD, THETA, sink.double().numpy())
+    assert_close_out(out, ro, torch.bfloat16)
+    assert_close_lse(lse, rl)
