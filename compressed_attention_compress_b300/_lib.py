@@ -214,7 +214,7 @@ def hsa_attn_decode_v4(q, kc, vc, m, idx, cnt, k_raw, v_raw, window, ctx_len, sc
     """hsa_attn_decode with the V4 query preparation (RMSNorm, partial RoPE) and the sink and
     inverse rotation of the output inside the attention kernel; q is the raw query."""
     B, H, d = q.shape
-    topk = idx.shape[-1]
+    topk = idx.shape[-1] if idx is not None else 0
     _chk(lib.hsa_attn_decode_v4(_p(q), _dt(q), B, H, d, _p(kc), _p(vc), kc.stride(0), kc.stride(1), kc.shape[1],
                                 int(m), _p(idx), _p(cnt), topk, _p(k_raw), _p(v_raw), k_raw.stride(0),
                                 k_raw.stride(1), k_raw.shape[1], int(window), _p(ctx_len), float(scale), _p(gamma_q),
