@@ -7,7 +7,7 @@
 // the barrier completes; each wait is still bounded and raises the device flag
 // if it ever gives up):
 //   phase 1  dp4a scores of this CTA's chunk, kept in shared memory as biased
-//            keys u = s + DI*16256; a 2048-bin histogram of u >> shift1 is
+//            keys u = s + DI*16256; a 1024-bin histogram of u >> shift1 is
 //            merged into the row's global histogram.               -- barrier
 //   phase 2  every CTA reads the row histogram and finds the bin b1 holding
 //            the k-th largest key; it writes its keys in bins >= b1 (key,
@@ -30,7 +30,7 @@ namespace hsa {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kNB1 = 2048;
+constexpr int kNB1 = 1024;                    // level-1 histogram bins
 constexpr unsigned long long kSpinLimit = 1ull << 24;
 constexpr int kStages = 3;
 constexpr int kStageBytes = 16384;
@@ -519,7 +519,7 @@ FusedIndexPlan plan_index_fused(int rows, int DI, int64_t E_cap, int num_sms) {
     if (rows <= 0 || E_cap <= 0) return p;
     p.rows = rows;
     p.key_bits = key_bits_for(DI);
-    p.shift1 = p.key_bits - 11;
+    p.shift1 = p.key_bits - 10;
     p.nb2 = 1 << p.shift1;
     // Chunks are multiples of 64 entries; pick the smallest chunk whose launch
     // (ceil(E/chunk) CTAs per row) is resident all at once, so every SM streams
