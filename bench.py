@@ -61,10 +61,10 @@ UNIT = "queries/s"
 # that capture ran (sha256 of each file).
 TRAFFIC = {
     ("index_fused_kernel", "pro_csa_decode"): {
-        "bytes": 67259136 + 525056,
+        "bytes": 67240960 + 509952,
         "sources": {
             "compressed_attention_compress_b300/csrc/index_fused.cu":
-                "12ae7fbe36b53fd0a7d4718beb4249787f0d1a074987417107b5f379e0cadd16",
+                "07a532c05edea268a0dd2b2fd8e9e3d7969f8ad7693ca4309344da283dddfc61",
             "compressed_attention_compress_b300/csrc/common.cuh":
                 "79620607484ca1168ae52da7bbf685b100d0e8e9f3444486c3871e963c3a346d",
             "compressed_attention_compress_b300/csrc/block_scan.cuh":
