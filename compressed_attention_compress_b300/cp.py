@@ -20,8 +20,10 @@ The exchange is written once, against two small interfaces: `allgather(t)`
 returns the rank-ordered stack of every rank's `t` (torch.distributed, or an
 emulation of several ranks in one process), and `ops` computes the per-rank
 steps.  `DeviceOps` runs them through the library's CUDA kernels (C ABI).
-Dense (HCA) layers shard the same way with step 2 left out; this module covers
-the CSA step.
+Dense (HCA) layers (QbitAI article, the HCA paragraph: dense attention over every
+compressed entry) shard the same way with steps 1-2 left out: every rank attends to
+all of its visible entries, the window rank adds the window, and the partials are
+merged (`cp_decode_step_dense`).
 """
 from __future__ import annotations
 
@@ -99,16 +101,37 @@ def cp_decode_step(sh: Shard, q: torch.Tensor, q_idx: torch.Tensor, ctx_len: tor
     return out, lse, sel
 
 
+def cp_decode_step_dense(sh: Shard, q: torch.Tensor, ctx_len: torch.Tensor, *, m: int, window: int, scale: float,
+                         allgather: Callable[[torch.Tensor], torch.Tensor], ops):
+    """One HCA decode step of B sequences (query at p = ctx_len - 1): every rank attends
+    to all of its visible entries (listed explicitly, so the same per-rank attention
+    serves), the window rank adds the raw window, and one all-gather of the partial
+    (out, lse) feeds the log-sum-exp merge.  `sh.k_idx` is not read.
+    Returns (out [B, H, d], lse [B, H] fp32)."""
+    B = q.shape[0]
+    E = torch.div(ctx_len, m, rounding_mode="floor")
+    E_loc = (E - sh.e0).clamp(min=0, max=sh.n_local).to(q.device)
+    ar = torch.arange(sh.n_local, dtype=torch.int32, device=q.device)
+    loc = torch.where(ar[None, :] < E_loc[:, None], ar[None, :].expand(B, -1),
+                      torch.full((B, sh.n_local), -1, dtype=torch.int32, device=q.device))
+    w = window if sh.rank == sh.window_rank else 0
+    o_r, lse_r = ops.attn_partial(q, sh.kc, sh.vc, m, loc.contiguous(), sh.k_raw, sh.v_raw, w, ctx_len, scale)
+    return ops.lse_merge(allgather(o_r), allgather(lse_r))
+
+
 class DeviceOps:
     """The per-rank steps on this process's GPU through the library's C ABI
     (workspaces are allocated once here and reused; the library allocates nothing)."""
 
     def __init__(self, B: int, H: int, d: int, DI: int, n_local: int, m: int, topk: int, window: int,
                  dtype=torch.bfloat16, device="cuda"):
+        """DI = 0: no indexer (the dense step); its attention lists every local entry,
+        so pass topk = n_local."""
         from . import _lib as L
         self.L = L
         self.topk = topk
-        self.ws_i = L.workspace(L.hsa_index_topk_workspace_size(B, 1, DI, n_local, topk), device=device)
+        self.ws_i = (L.workspace(L.hsa_index_topk_workspace_size(B, 1, DI, n_local, topk), device=device)
+                     if DI else None)
         self.ws_a = L.workspace(L.hsa_attn_decode_workspace_size(dtype, B, H, d, n_local, m, topk, window),
                                 device=device)
 

@@ -139,3 +139,12 @@ def full_reference(x, ctx_len, m, topk, window, scale):
     idx, cnt = oracle.index_topk_rows(x["q_idx"][:, 0], np.arange(B), p, x["k_idx"], m, topk)
     o, l = oracle.attn_rows(x["q"], np.arange(B), p, x["kc"], x["vc"], m, idx, x["k_raw"], x["v_raw"], window, scale)
     return idx, o, l
+
+
+def full_reference_dense(x, ctx_len, m, window, scale):
+    """Single-process oracle of the HCA step: attention over every visible entry."""
+    B = x["q"].shape[0]
+    p = np.asarray(ctx_len) - 1
+    o, l = oracle.attn_rows(x["q"], np.arange(B), p, x["kc"], x["vc"], m, None, x["k_raw"], x["v_raw"], window,
+                            scale)
+    return o, l

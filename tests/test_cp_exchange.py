@@ -1,7 +1,8 @@
 """Context-parallel exchange of one long sequence (entry sharding across ranks):
-the protocol of cp.cp_decode_step run by 2 gloo ranks in separate processes and
-by 3-4 ranks emulated as threads, with the per-rank steps computed by the oracle,
-against the single-process oracle of the same decode step."""
+the protocols of cp.cp_decode_step (CSA) and cp.cp_decode_step_dense (HCA) run by
+2 gloo ranks in separate processes and by 1-4 ranks emulated as threads, with the
+per-rank steps computed by the oracle, against the single-process oracle of the
+same decode step."""
 import os
 import socket
 
@@ -12,9 +13,10 @@ import torch.multiprocessing as mp
 
 import oracle
 from compressed_attention_compress_b300 import cp
-from tests.cp_testlib import OracleOps, ThreadGroup, cp_case, full_reference
+from tests.cp_testlib import OracleOps, ThreadGroup, cp_case, full_reference, full_reference_dense
 
 M, H, D, DI, TOPK, W = 4, 4, 16, 32, 8, 8
+M_HCA = 16          # HCA-layer block size of the dense cases (the window W < M_HCA)
 SCALE = 1.0 / np.sqrt(D)
 
 
@@ -33,6 +35,20 @@ def _run_rank(rank, world, x, E_cap, ctx, allgather, window_rank):
                              allgather=allgather, ops=ops)
 
 
+def _run_rank_dense(rank, world, x, E_cap, ctx, allgather, window_rank):
+    sh = _shard(x, world, rank, E_cap, window_rank)
+    ops = OracleOps(sh.e0, E_cap)
+    return cp.cp_decode_step_dense(sh, torch.from_numpy(x["q"]), torch.tensor(ctx, dtype=torch.int64), m=M_HCA,
+                                   window=W, scale=SCALE, allgather=allgather, ops=ops)
+
+
+def _check_dense(res, x, ctx):
+    ref_o, ref_l = full_reference_dense(x, ctx, M_HCA, W, SCALE)
+    for out, lse in res:
+        np.testing.assert_allclose(out.numpy(), ref_o, atol=1e-10, rtol=0)
+        np.testing.assert_allclose(lse.numpy(), ref_l, atol=1e-10, rtol=0)
+
+
 def _check(res, x, ctx):
     ref_idx, ref_o, ref_l = full_reference(x, ctx, M, TOPK, W, SCALE)
     for out, lse, sel in res:
@@ -49,13 +65,27 @@ CASES = [
 ]
 
 
-def _gloo_worker(rank, world, port, case):
+DENSE_CASES = [
+    # (seed, B, E_cap, ctx_len per sequence)
+    (21, 2, 24, [384, 384]),              # every entry visible
+    (22, 3, 24, [200, 384, 15]),          # rank 1's entries not visible for sequence 0; no entry at all for 2
+    (23, 1, 5, [75]),                     # 5 entries: ragged shards, an empty one on 4 ranks; a partial block
+]
+
+
+def _gloo_worker(rank, world, port, case, dense=False):
     os.environ["MASTER_ADDR"] = "127.0.0.1"
     os.environ["MASTER_PORT"] = str(port)
     import torch.distributed as dist
     dist.init_process_group("gloo", rank=rank, world_size=world)
     try:
         oracle.build()
+        if dense:
+            seed, B, E_cap, ctx = case
+            x = cp_case(seed, B, E_cap, M_HCA, H, D, DI)
+            res = _run_rank_dense(rank, world, x, E_cap, ctx, cp.torch_allgather(), window_rank=world - 1)
+            _check_dense([res], x, ctx)
+            return
         seed, B, E_cap, ctx, ties = case
         x = cp_case(seed, B, E_cap, M, H, D, DI, ties)
         res = _run_rank(rank, world, x, E_cap, ctx, cp.torch_allgather(), window_rank=world - 1)
@@ -85,6 +115,23 @@ def test_cp_thread_ranks(case, world):
     tg = ThreadGroup(world)
     res = tg.run(lambda r, ag: _run_rank(r, world, x, E_cap, ctx, ag, window_rank=0))
     _check(res, x, ctx)
+
+
+@pytest.mark.parametrize("case", DENSE_CASES, ids=["full", "short", "ragged"])
+def test_cp_dense_gloo_two_ranks(case):
+    oracle.build()
+    mp.spawn(_gloo_worker, args=(2, _free_port(), case, True), nprocs=2, join=True)
+
+
+@pytest.mark.parametrize("world", [1, 3, 4])
+@pytest.mark.parametrize("case", DENSE_CASES, ids=["full", "short", "ragged"])
+def test_cp_dense_thread_ranks(case, world):
+    oracle.build()
+    seed, B, E_cap, ctx = case
+    x = cp_case(seed, B, E_cap, M_HCA, H, D, DI)
+    tg = ThreadGroup(world)
+    res = tg.run(lambda r, ag: _run_rank_dense(r, world, x, E_cap, ctx, ag, window_rank=world // 2))
+    _check_dense(res, x, ctx)
 
 
 def test_cp_union_of_local_topk_is_global_topk():

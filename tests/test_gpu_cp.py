@@ -1,7 +1,7 @@
 """GPU parity of the context-parallel exchange kernels (hsa_index_scores,
-hsa_topk_merge, hsa_lse_merge) against their definitions, and the CP decode step
-on the GPU (ranks emulated as threads of one process, per-rank steps through the
-C ABI) against the single-GPU path and the oracle."""
+hsa_topk_merge, hsa_lse_merge) against their definitions, and the CSA and HCA CP
+decode steps on the GPU (ranks emulated as threads of one process, per-rank steps
+through the C ABI) against the single-GPU path and the oracle."""
 import numpy as np
 import pytest
 import torch
@@ -138,6 +138,45 @@ def test_cp_decode_step_device(L, world):
                               host_np(k_raw), host_np(v_raw), W, scale)
     for out, lse, sel in res:
         assert np.array_equal(sel.cpu().numpy(), ref_idx)
+        assert_close_out(out, ro, torch.bfloat16)
+        assert_close_lse(lse, rl)
+    L.hsa_check()
+
+
+@pytest.mark.parametrize("world", [1, 2, 4])
+def test_cp_decode_step_dense_device(L, world):
+    """HCA shape (m = 128, 128-token window) on a 256k-token context: each rank's
+    attention over all its visible entries, merged, matches the oracle of the
+    unsharded dense step (one rank's list exceeds the tensor-core kernel's 2,048
+    slots at world 1, so the general kernel is covered too)."""
+    B, H, d, m, W = 2, 64, 128, 128, 128
+    E_cap = 2048
+    N = E_cap * m
+    dev = torch.device("cuda")
+    g = torch.Generator().manual_seed(60 + world)
+    kc = torch.randn((B, E_cap, d), generator=g).to(torch.bfloat16)
+    vc = torch.randn((B, E_cap, d), generator=g).to(torch.bfloat16)
+    k_raw = torch.randn((B, N, d), generator=g).to(torch.bfloat16)
+    v_raw = torch.randn((B, N, d), generator=g).to(torch.bfloat16)
+    q = torch.randn((B, H, d), generator=g).to(torch.bfloat16)
+    ctx = torch.tensor([N, N // 3 + 77], dtype=torch.int64)   # the second stops inside rank 0's or 1's range
+    scale = 1.0 / d ** 0.5
+
+    def rank_fn(r, ag):
+        e0, e1 = cp.shard_bounds(E_cap, world, r)
+        sh = cp.Shard(rank=r, world=world, e0=e0, kc=kc[:, e0:e1].contiguous().to(dev),
+                      vc=vc[:, e0:e1].contiguous().to(dev), k_idx=torch.empty(0, dtype=torch.int8, device=dev),
+                      k_raw=k_raw.to(dev), v_raw=v_raw.to(dev), window_rank=0)
+        ops = cp.DeviceOps(B, H, d, 0, e1 - e0, m, e1 - e0, W)
+        out, lse = cp.cp_decode_step_dense(sh, q.to(dev), ctx.to(dev), m=m, window=W, scale=scale,
+                                           allgather=ag, ops=ops)
+        torch.cuda.synchronize()
+        return out, lse
+
+    res = ThreadGroup(world).run(rank_fn)
+    ro, rl = oracle.attn_rows(host_np(q), np.arange(B), ctx.numpy() - 1, host_np(kc), host_np(vc), m, None,
+                              host_np(k_raw), host_np(v_raw), W, scale)
+    for out, lse in res:
         assert_close_out(out, ro, torch.bfloat16)
         assert_close_lse(lse, rl)
     L.hsa_check()
