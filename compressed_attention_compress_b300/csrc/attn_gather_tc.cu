@@ -16,9 +16,13 @@
 //              O rescaled in TMEM only when the maximum grows by > 2^8.
 //   warps 4-7  gather: each thread resolves one item row of tile j (selected entry
 //              of Kc/Vc or window token of the raw cache, zero-filled when
-//              invalid); half-warps then copy whole 256-byte rows with 16-byte
-//              cp.async into a 5-slot ring of 32 KiB 128-byte-swizzled tiles; a
+//              invalid) into a 5-slot ring of 32 KiB 128-byte-swizzled tiles; a
 //              128-bit validity mask per tile goes to a small ring of its own.
+//              Rows are copied either by the tensor-memory-access unit, four rows
+//              per `cp.async.bulk.tensor` `tile::gather4` instruction (one per
+//              64-column half; row coordinates into the cache viewed as a 2-D
+//              tensor, tensor maps one row high), or, where the caches' strides
+//              do not allow that view, by half-warps with 16-byte `cp.async`.
 //              Thread 0 of the group also loads each token's Q by TMA.
 //   warp 8     MMA issuer (one thread): S(g) into one of two TMEM buffers, then
 //              O += P(g-1) V(g-1); completion via tcgen05.commit.
@@ -45,8 +49,13 @@ constexpr int kTBlk = kN * 128;            // 16 KiB per 64-column block of a ti
 constexpr int kRing = 5;
 constexpr int kMaskRing = 8;
 constexpr int kSoftWarps = 4, kGatherWarps = 4;
-constexpr int kThreads = (kSoftWarps + kGatherWarps + 1) * 32;
 constexpr int kGatherThreads = kGatherWarps * 32;
+constexpr int kKWarps = 4, kVWarps = 2;  // tile::gather4 variant: K-copy and V-copy warps
+// warps: softmax, gather (4, or 4 K + 2 V), MMA issuer
+template <bool kTma>
+constexpr int kThreadsOf = (kSoftWarps + (kTma ? kKWarps + kVWarps : kGatherWarps) + 1) * 32;
+template <bool kTma>
+constexpr int kMmaWarpOf = kSoftWarps + (kTma ? kKWarps + kVWarps : kGatherWarps);
 constexpr int kLag = 3;       // cp.async groups a gather thread keeps in flight: the MMA takes
                               // K_{g+1} before releasing V_g, so kLag <= kRing - 2 keeps the ring live
 constexpr float kLog2e = 1.4426950408889634f;
@@ -65,6 +74,7 @@ struct __align__(8) Bars {
 struct GatherArgs {
     int rows, T, topk, window, m, n_tiles;
     int64_t E_cap, N_cap, c_sb, c_se, r_sb, r_st;
+    int64_t c_rows_b, r_rows_b;  // row-coordinate step per sequence of the 2-D cache views (c_sb / c_se, r_sb / r_st)
     const int64_t *q_pos0;
     const int32_t *idx, *cnt;
     const __nv_bfloat16 *kc, *vc, *k_raw, *v_raw;
@@ -85,6 +95,9 @@ __device__ __forceinline__ bool wait_bar(uint64_t *bar, unsigned parity, volatil
 __device__ __forceinline__ void arrive(uint64_t *bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(smem_u32(bar)) : "memory");
 }
+__device__ __forceinline__ void arrive2(uint64_t *bar) {  // two arrivals at once
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0], 2;\n" ::"r"(smem_u32(bar)) : "memory");
+}
 __device__ __forceinline__ uint64_t fma_f32x2(uint64_t x, uint64_t y, uint64_t z) {
     uint64_t d;
     asm("fma.rn.f32x2 %0, %1, %2, %3;\n" : "=l"(d) : "l"(x), "l"(y), "l"(z));
@@ -100,13 +113,28 @@ __device__ __forceinline__ uint64_t pack2(float lo, float hi) {
 }
 __device__ __forceinline__ float lo_of(uint64_t v) { return __uint_as_float((uint32_t)v); }
 __device__ __forceinline__ float hi_of(uint64_t v) { return __uint_as_float((uint32_t)(v >> 32)); }
+// Four rows (r0..r3) of a 2-D tensor, columns [x, x + box width), into 4 consecutive
+// box rows at dst, counted in bytes on bar.
+__device__ __forceinline__ void tma_gather4(void *dst, const CUtensorMap *tm, int x, int r0, int r1, int r2, int r3,
+                                            uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes [%0], "
+        "[%1, {%2, %3, %4, %5, %6}], [%7];\n" ::"r"(smem_u32(dst)),
+        "l"(tm), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(smem_u32(bar))
+        : "memory");
+}
 template <int N>
 __device__ __forceinline__ void cp_wait() {
     asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
-    attn_gather_tc_kernel(const __grid_constant__ CUtensorMap tm_q, GatherArgs a) {
+// kTma: rows by tile::gather4 (tm_kc, tm_vc, tm_kr, tm_vr: the caches as 2-D tensors of
+// d-wide rows, boxes of 64 columns x 1 row); otherwise by cp.async (those maps unused).
+template <bool kTma>
+__global__ void __launch_bounds__(kThreadsOf<kTma>, 1)
+    attn_gather_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kc,
+                          const __grid_constant__ CUtensorMap tm_vc, const __grid_constant__ CUtensorMap tm_kr,
+                          const __grid_constant__ CUtensorMap tm_vr, GatherArgs a) {
     extern __shared__ __align__(16) unsigned char smem_raw[];  // rounded up to 1024 at run time
     unsigned char *smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
     unsigned char *sQ = smem;                          // 2 x 16 KiB
@@ -126,11 +154,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&bars.s_free[i], kSoftWarps * 32);
         }
         for (int i = 0; i < kRing; ++i) {
-            mbar_init(&bars.kv_full[i], kGatherThreads);
+            mbar_init(&bars.kv_full[i], kGatherThreads);  // V threads of the gather4 variant arrive twice
             mbar_init(&bars.kv_empty[i], 1);
         }
         for (int i = 0; i < kMaskRing; ++i) {
-            mbar_init(&bars.m_full[i], kGatherWarps);
+            mbar_init(&bars.m_full[i], kTma ? kVWarps : kGatherWarps);
             mbar_init(&bars.m_empty[i], kSoftWarps * 32);
         }
         mbar_init(&bars.p_full, kSoftWarps * 32);
@@ -145,12 +173,192 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc::fence_after();
     const uint32_t tmem = s_tmem;
-    const uint32_t tS[2] = {tmem, tmem + 128};
+    auto tS = [tmem](int64_t gg) -> uint32_t { return tmem + (uint32_t)(gg & 1) * 128u; };  // S double buffer
     const uint32_t tO = tmem + 256;
     const int nt = a.n_tiles;
 
-    if (warp >= kSoftWarps && warp < kSoftWarps + kGatherWarps) {
-        // ---------------------------------------------------------------- gather
+    if (kTma && warp >= kSoftWarps && warp < kMmaWarpOf<kTma>) {
+        // ------------------------------------------------------ gather (two engines)
+        // Warps 4-7 copy K tiles with tile::gather4 (the tensor-memory-access unit; a warp's
+        // gather4 lanes issue one after another, so four warps share the K rows), warps 8-9
+        // copy V tiles with cp.async (the load/store unit), so the two engines work in
+        // parallel.  Each group resolves every row of a tile itself (K warp w: row 32w + t;
+        // V warp w: rows 64w + t and 64w + 32 + t), so the groups only meet at the ring's
+        // barriers.  Groups of 4 rows go to one gather4: an invalid row copies a valid row of
+        // its group (its logits are masked, so it adds nothing), a group with no valid row is
+        // zeroed instead; valid rows of one group share a cache because topk is a multiple of 4.
+        const int gw = warp - kSoftWarps;
+        const bool k_role = gw < kKWarps;
+        const int w2 = k_role ? gw : gw - kKWarps;
+        const int R1 = k_role ? 32 * w2 + lane : 64 * w2 + lane, R2 = R1 + 32;  // this thread's rows
+        int it = 0;
+        int64_t g = 0;  // item tiles
+        bool ok = true;
+        // slot i of the row's list: the selected entry or window token, its address (V), its row
+        // coordinate in the 2-D view of its cache and which cache (K); false when invalid
+        auto resolve = [&](int b, int64_t p, int64_t E, int slot_i, int32_t e, const __nv_bfloat16 *&vp, int &crd,
+                           int &raw) -> bool {
+            vp = nullptr;
+            crd = 0;
+            raw = 0;
+            if (slot_i < a.topk) {
+                if (e >= E) raise_flag(FLAG_ATTN_INDEX);
+                if (e >= 0 && e < E) {
+                    vp = a.vc + b * a.c_sb + (int64_t)e * a.c_se;
+                    crd = (int)(b * a.c_rows_b + e);
+                    return true;
+                }
+            } else if (slot_i < a.topk + a.window) {
+                const int64_t tr = p - a.window + 1 + (slot_i - a.topk);
+                if (tr >= 0 && tr <= p) {
+                    if (tr >= a.N_cap) {
+                        raise_flag(FLAG_ATTN_RANGE);
+                    } else {
+                        vp = a.v_raw + b * a.r_sb + tr * a.r_st;
+                        crd = (int)(b * a.r_rows_b + tr);
+                        raw = 1;
+                        return true;
+                    }
+                }
+            }
+            return false;
+        };
+        // the four row coordinates of this lane's group (lanes 4q..4q+3), invalid rows replaced
+        auto group = [&](bool v, int crd, int raw, int (&c4)[4], int &graw) -> uint32_t {
+            const uint32_t bits = __ballot_sync(0xffffffffu, v);
+            const uint32_t gb = (bits >> (lane & ~3)) & 0xFu;
+            const int src = (lane & ~3) + (gb ? __ffs(gb) - 1 : 0);
+            const int sc = __shfl_sync(0xffffffffu, crd, src);
+            graw = __shfl_sync(0xffffffffu, raw, src);
+            const int mine = v ? crd : sc;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) c4[i] = __shfl_sync(0xffffffffu, mine, (lane & ~3) + i);
+            return gb;
+        };
+        for (int row = blockIdx.x; row < a.rows && ok; row += gridDim.x, ++it) {
+            const int b = row / a.T, t = row - (row / a.T) * a.T;
+            const int64_t p = a.q_pos0[b] + t;
+            int64_t E = num_entries(p, a.m);
+            if (E > a.E_cap) E = a.E_cap;
+            const int cntr = a.cnt ? min(max(a.cnt[row], 0), a.topk) : a.topk;
+            if (gw == 0 && lane == 0) {
+                if (it >= 2) ok = wait_bar(&bars.q_empty[it & 1], (unsigned)(((it >> 1) - 1) & 1), &s_abort);
+                if (ok) {
+                    mbar_expect_tx(&bars.q_full[it & 1], kQBytes);
+                    tc::tma_load_2d(sQ + (it & 1) * kQBytes, &tm_q, 0, row * kH, &bars.q_full[it & 1]);
+                    tc::tma_load_2d(sQ + (it & 1) * kQBytes + kQBlk, &tm_q, 64, row * kH, &bars.q_full[it & 1]);
+                }
+            }
+            ok = __all_sync(0xffffffffu, ok);
+            auto sel = [&](int slot_i) -> int32_t {
+                return (slot_i < a.topk && slot_i < cntr) ? a.idx[(int64_t)row * a.topk + slot_i] : -1;
+            };
+            // selected indices one tile ahead, so each load's round trip overlaps the copies
+            int32_t n1 = sel(R1), n2 = k_role ? -1 : sel(R2);
+            for (int j = 0; j < nt && ok; ++j, ++g) {
+                const int s1 = j * kN + R1, s2 = j * kN + R2;
+                const int32_t e1 = n1, e2 = n2;
+                n1 = sel(s1 + kN);
+                if (!k_role) n2 = sel(s2 + kN);
+                const __nv_bfloat16 *vp1, *vp2 = nullptr;
+                int crd1, raw1, crd2 = 0, raw2 = 0;
+                const bool v1 = resolve(b, p, E, s1, e1, vp1, crd1, raw1);
+                const bool v2 = k_role ? false : resolve(b, p, E, s2, e2, vp2, crd2, raw2);
+                if (k_role) {
+                    int c4a[4], graw1;
+                    const uint32_t gb1 = group(v1, crd1, raw1, c4a, graw1);
+                    const int64_t uk = 2 * g;
+                    const int sk = (int)(uk % kRing);
+                    if (uk >= kRing) ok = wait_bar(&bars.kv_empty[sk], (unsigned)(((uk / kRing) - 1) & 1), &s_abort);
+                    ok = __all_sync(0xffffffffu, ok);
+                    if (!ok) break;
+                    unsigned char *dK = sRing + sk * kTile;
+                    if (gb1 == 0) {
+#pragma unroll
+                        for (int c = 0; c < 8; ++c) {
+                            *reinterpret_cast<uint4 *>(dK + R1 * 128 + c * 16) = make_uint4(0, 0, 0, 0);
+                            *reinterpret_cast<uint4 *>(dK + kTBlk + R1 * 128 + c * 16) = make_uint4(0, 0, 0, 0);
+                        }
+                        tc::fence_proxy_async();  // generic zeros before the MMA reads the tile
+                    }
+                    const uint32_t l1 = __ballot_sync(0xffffffffu, (lane & 3) == 0 && gb1 != 0);
+                    __syncwarp();
+                    // one arrival per K thread; lane 0 of each warp brings that warp's bytes
+                    // before the warp's copies issue
+                    if (lane == 0) mbar_expect_tx(&bars.kv_full[sk], (unsigned)__popc(l1) * 1024u);
+                    else arrive(&bars.kv_full[sk]);
+                    __syncwarp();
+                    if ((l1 >> lane) & 1u) {
+                        const CUtensorMap *tm = graw1 ? &tm_kr : &tm_kc;
+                        tma_gather4(dK + R1 * 128, tm, 0, c4a[0], c4a[1], c4a[2], c4a[3], &bars.kv_full[sk]);
+                        tma_gather4(dK + kTBlk + R1 * 128, tm, 64, c4a[0], c4a[1], c4a[2], c4a[3], &bars.kv_full[sk]);
+                    }
+                } else {
+                    // validity mask of the tile: words 2w and 2w + 1 (rows 64w.., 64w + 32..)
+                    const uint32_t b1 = __ballot_sync(0xffffffffu, v1), b2 = __ballot_sync(0xffffffffu, v2);
+                    const int ms = (int)(g % kMaskRing);
+                    if (g >= kMaskRing)
+                        ok = wait_bar(&bars.m_empty[ms], (unsigned)(((g / kMaskRing) - 1) & 1), &s_abort);
+                    ok = __all_sync(0xffffffffu, ok);
+                    if (!ok) break;
+                    if (lane == 0) {
+                        s_mask[ms][2 * w2] = b1;
+                        s_mask[ms][2 * w2 + 1] = b2;
+                        arrive(&bars.m_full[ms]);
+                    }
+                    const int64_t uv = 2 * g + 1;
+                    const int sv = (int)(uv % kRing);
+                    if (uv >= kRing) ok = wait_bar(&bars.kv_empty[sv], (unsigned)(((uv / kRing) - 1) & 1), &s_abort);
+                    ok = __all_sync(0xffffffffu, ok);
+                    if (!ok) break;
+                    // a half-warp copies one 256-byte row (lane l: 16-byte chunk l % 16), two
+                    // rows per instruction; row pointers come by shuffle from the resolving lane
+                    unsigned char *dV = sRing + sv * kTile;
+                    const unsigned long long a1 = reinterpret_cast<unsigned long long>(vp1);
+                    const unsigned long long a2 = reinterpret_cast<unsigned long long>(vp2);
+                    const int c = lane & 15;
+#pragma unroll 4
+                    for (int i = 0; i < 32; ++i) {
+                        const int rl = 2 * (i & 15) + (lane >> 4);
+                        const unsigned long long rs = __shfl_sync(0xffffffffu, i < 16 ? a1 : a2, rl);
+                        const int rr = 64 * w2 + (i < 16 ? 0 : 32) + rl;  // row within the tile
+                        const uint32_t off = (uint32_t)((c >> 3) * kTBlk + rr * 128 + (((c & 7) ^ (rr & 7)) << 4));
+                        const __nv_bfloat16 *rp = reinterpret_cast<const __nv_bfloat16 *>(rs);
+                        cp_async_16(smem_u32(dV + off), rp ? (const void *)(rp + c * 8) : (const void *)a.vc,
+                                    rp ? 16 : 0);  // zero-fill invalid rows
+                    }
+                    cp_async_commit();
+                    // the previous tile's V has landed once at most this tile's copies are pending
+                    // (each V thread stands for two of the barrier's 128 arrivals)
+                    if (g > 0) {
+                        cp_wait<1>();
+                        tc::fence_proxy_async();
+                        arrive2(&bars.kv_full[(uv - 2) % kRing]);
+                    }
+                }
+            }
+        }
+        if (!ok) s_abort = 1;
+        if (k_role) {
+            // the last two K tiles' slots are not reused: their copies land before the CTA exits
+            // (normally the MMA has already consumed them)
+            if (lane == 0) {
+                volatile int never = 0;
+                for (int64_t h = (g > 2 ? g - 2 : 0); h < g; ++h)
+                    wait_bar(&bars.kv_full[(2 * h) % kRing], (unsigned)(((2 * h) / kRing) & 1), &never);
+            }
+            if (gw == 0 && lane == 0 && it > 0) {
+                volatile int never = 0;
+                wait_bar(&bars.q_full[(it - 1) & 1], (unsigned)(((it - 1) >> 1) & 1), &never);
+            }
+        } else {
+            // publish the last V tile
+            cp_wait<0>();
+            tc::fence_proxy_async();
+            if (g > 0) arrive2(&bars.kv_full[(2 * (g - 1) + 1) % kRing]);
+        }
+    } else if (!kTma && warp >= kSoftWarps && warp < kMmaWarpOf<kTma>) {
+        // ------------------------------------------------------- gather (cp.async)
         const int gt = threadIdx.x - kSoftWarps * 32;  // 0..127: the item row this thread copies
         const int gw = gt >> 5;
         int it = 0;
@@ -252,7 +460,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             volatile int never = 0;
             wait_bar(&bars.q_full[(it - 1) & 1], (unsigned)(((it - 1) >> 1) & 1), &never);
         }
-    } else if (warp == kSoftWarps + kGatherWarps) {
+    } else if (warp == kMmaWarpOf<kTma>) {
         // ------------------------------------------------------------- MMA issuer
         if (lane == 0) {
             constexpr uint32_t idS = tc::idesc_bf16(kH, kN, false, false);
@@ -298,7 +506,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int kk = 0; kk < kD / 16; ++kk) {
                         const uint64_t da = tc::desc_sw128(aQ + (kk >> 2) * kQBlk + (kk & 3) * 32, 16, 1024);
                         const uint64_t db = tc::desc_sw128(aK + (kk >> 2) * kTBlk + (kk & 3) * 32, 16, 1024);
-                        tc::mma_bf16(tS[g & 1], da, db, idS, kk > 0 ? 1u : 0u);
+                        tc::mma_bf16(tS(g), da, db, idS, kk > 0 ? 1u : 0u);
                     }
                     tc::commit(&bars.s_full[g & 1]);
                     tc::commit(&bars.kv_empty[uk % kRing]);
@@ -344,7 +552,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int q = 0; q < 2; ++q) {
                     uint32_t w[32];
-                    tc::tmem_ld32(tS[g & 1] + lane_off + 64 + q * 32, w);
+                    tc::tmem_ld32(tS(g) + lane_off + 64 + q * 32, w);
                     tc::tmem_wait_ld();
 #pragma unroll
                     for (int c = 0; c < 32; ++c) v[q * 32 + c] = __shfl_xor_sync(0xffffffffu, w[c], 16);
@@ -352,7 +560,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int q = 0; q < 2; ++q) {
                     uint32_t w[32];
-                    tc::tmem_ld32(tS[g & 1] + lane_off + q * 32, w);
+                    tc::tmem_ld32(tS(g) + lane_off + q * 32, w);
                     tc::tmem_wait_ld();
 #pragma unroll
                     for (int c = 0; c < 32; ++c) v[q * 32 + c] = upper ? v[q * 32 + c] : w[c];
@@ -384,6 +592,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                     l *= (m_used == -INFINITY) ? 0.f : alpha;
                     m_used = mx;
                 }
+                // P = 2^(x * scale_log2 - m_used) in bf16 (each lane its 64 columns), computed
+                // in registers while the previous PV still reads P; invalid items read as -inf
+                // (exponent 0), the scale goes into a packed FMA
+                const float nmu = m_used == -INFINITY ? 0.f : -m_used;
+                const uint64_t nmu2 = pack2(nmu, nmu), sc2 = pack2(a.scale_log2, a.scale_log2);
+                uint64_t acc2[4] = {0, 0, 0, 0};
+                uint32_t pk[32];
+#pragma unroll
+                for (int c2 = 0; c2 < 32; ++c2) {
+                    const uint64_t arg = fma_f32x2(((uint64_t)v[2 * c2 + 1] << 32) | v[2 * c2], sc2, nmu2);
+                    const float p0 = tc::ex2(lo_of(arg)), p1 = tc::ex2(hi_of(arg));
+                    acc2[c2 & 3] = add_f32x2(acc2[c2 & 3], pack2(p0, p1));
+                    pk[c2] = pack_bf16x2(p0, p1);
+                }
                 // P and O are free once the previous PV has completed
                 if (g > 0) ok = wait_bar(&bars.o_done, (unsigned)((g - 1) & 1), &s_abort);
                 ok = __all_sync(0xffffffffu, ok);
@@ -401,26 +623,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     tc::tmem_wait_st();
                 }
-                // P = 2^(x * scale_log2 - m_used) in bf16, 128-byte-swizzled K-major rows (each
-                // lane its 64 columns); invalid items read as -inf (exponent 0), the scale goes
-                // into a packed FMA
-                const float nmu = m_used == -INFINITY ? 0.f : -m_used;
-                const uint64_t nmu2 = pack2(nmu, nmu), sc2 = pack2(a.scale_log2, a.scale_log2);
-                uint64_t acc2[4] = {0, 0, 0, 0};
+                // P into 128-byte-swizzled K-major rows
 #pragma unroll
-                for (int cc = 0; cc < 8; ++cc) {
-                    uint32_t pk[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int c0 = cc * 8 + 2 * e;
-                        const uint64_t arg = fma_f32x2(((uint64_t)v[c0 + 1] << 32) | v[c0], sc2, nmu2);
-                        const float p0 = tc::ex2(lo_of(arg)), p1 = tc::ex2(hi_of(arg));
-                        acc2[e] = add_f32x2(acc2[e], pack2(p0, p1));
-                        pk[e] = pack_bf16x2(p0, p1);
-                    }
+                for (int cc = 0; cc < 8; ++cc)
                     *reinterpret_cast<uint4 *>(sP + (upper ? kQBlk : 0) + hr * 128 + ((cc ^ (hr & 7)) << 4)) =
-                        make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                }
+                        make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
                 const uint64_t s4 = add_f32x2(add_f32x2(acc2[0], acc2[1]), add_f32x2(acc2[2], acc2[3]));
                 float sum = lo_of(s4) + hi_of(s4);
                 sum += __shfl_xor_sync(0xffffffffu, sum, 16);
@@ -504,11 +711,39 @@ cudaError_t launch_attn_gather_tc(const AttnArgs &a, int num_sms, cudaStream_t s
     g.scale_log2 = a.scale * kLog2e;
     g.out = static_cast<__nv_bfloat16 *>(a.out);
     g.lse = a.lse;
-    static unsigned long long done = 0;
-    cudaError_t e = smem_limit_once(attn_gather_tc_kernel, (int)kSmemBytes, done);
-    if (e != cudaSuccess) return e;
+    // Rows by tile::gather4 when each cache is a 2-D tensor of rows (a sequence's first row
+    // a whole number of rows after the previous one's), every row coordinate fits 31 bits,
+    // and a gather group of 4 slots never spans the selected entries and the window.
+    const int B = a.rows / a.T;
+    const bool strides_ok = a.c_se > 0 && a.c_sb % a.c_se == 0 && a.r_st > 0 && a.r_sb % a.r_st == 0;
+    CUtensorMap tkc = tq, tvc = tq, tkr = tq, tvr = tq;
+    bool tma = a.topk % 4 == 0 && strides_ok;
+    if (tma) {
+        g.c_rows_b = a.c_sb / a.c_se;
+        g.r_rows_b = a.r_sb / a.r_st;
+        const int64_t c_rows = (int64_t)(B - 1) * g.c_rows_b + a.E_cap;
+        const int64_t r_rows = (int64_t)(B - 1) * g.r_rows_b + a.N_cap;
+        tma = c_rows > 0 && r_rows > 0 && c_rows < (int64_t)INT32_MAX && r_rows < (int64_t)INT32_MAX;
+        if (tma) {
+            const uint64_t cd[2] = {(uint64_t)kD, (uint64_t)c_rows}, rd[2] = {(uint64_t)kD, (uint64_t)r_rows};
+            const uint64_t cs[1] = {(uint64_t)a.c_se}, rs[1] = {(uint64_t)a.r_st};
+            tma = make_tmap_bf16(&tkc, a.kc, 2, cd, cs, 1) && make_tmap_bf16(&tvc, a.vc, 2, cd, cs, 1) &&
+                  make_tmap_bf16(&tkr, a.k_raw, 2, rd, rs, 1) && make_tmap_bf16(&tvr, a.v_raw, 2, rd, rs, 1);
+        }
+    }
+    if (!tma) g.c_rows_b = g.r_rows_b = 0;
     const int grid = a.rows < num_sms ? a.rows : num_sms;
-    attn_gather_tc_kernel<<<grid, kThreads, kSmemBytes, s>>>(tq, g);
+    if (tma) {
+        static unsigned long long done = 0;
+        cudaError_t e = smem_limit_once(attn_gather_tc_kernel<true>, (int)kSmemBytes, done);
+        if (e != cudaSuccess) return e;
+        attn_gather_tc_kernel<true><<<grid, kThreadsOf<true>, kSmemBytes, s>>>(tq, tkc, tvc, tkr, tvr, g);
+    } else {
+        static unsigned long long done = 0;
+        cudaError_t e = smem_limit_once(attn_gather_tc_kernel<false>, (int)kSmemBytes, done);
+        if (e != cudaSuccess) return e;
+        attn_gather_tc_kernel<false><<<grid, kThreadsOf<false>, kSmemBytes, s>>>(tq, tkc, tvc, tkr, tvr, g);
+    }
     return cudaGetLastError();
 }
 
