@@ -24,8 +24,9 @@
 //              tensor, tensor maps one row high), or, where the caches' strides
 //              do not allow that view, by half-warps with 16-byte `cp.async`.
 //              Thread 0 of the group also loads each token's Q by TMA.
-//   warp 8     MMA issuer (one thread): S(g) into one of two TMEM buffers, then
-//              O += P(g-1) V(g-1); completion via tcgen05.commit.
+//   last warp  MMA issuer (one thread): S(g) into one of two TMEM buffers, then
+//              O += P(g-1) V(g-1) (g counted over all the CTA's tokens); completion via
+//              tcgen05.commit.
 // All waits are bounded; a wait that gives up raises the device flag and the CTA
 // stops issuing work.
 #include <math.h>
@@ -50,8 +51,8 @@ constexpr int kRing = 5;
 constexpr int kMaskRing = 8;
 constexpr int kSoftWarps = 4, kGatherWarps = 4;
 constexpr int kGatherThreads = kGatherWarps * 32;
-constexpr int kKWarps = 4, kVWarps = 2;  // tile::gather4 variant: K-copy and V-copy warps
-// warps: softmax, gather (4, or 4 K + 2 V), MMA issuer
+constexpr int kKWarps = 4, kVWarps = 3;  // tile::gather4 variant: K-copy and V-copy warps
+// warps: softmax, gather (4, or 4 K + 3 V), MMA issuer
 template <bool kTma>
 constexpr int kThreadsOf = (kSoftWarps + (kTma ? kKWarps + kVWarps : kGatherWarps) + 1) * 32;
 template <bool kTma>
@@ -154,11 +155,11 @@ __global__ void __launch_bounds__(kThreadsOf<kTma>, 1)
             mbar_init(&bars.s_free[i], kSoftWarps * 32);
         }
         for (int i = 0; i < kRing; ++i) {
-            mbar_init(&bars.kv_full[i], kGatherThreads);  // V threads of the gather4 variant arrive twice
+            mbar_init(&bars.kv_full[i], kGatherThreads);
             mbar_init(&bars.kv_empty[i], 1);
         }
         for (int i = 0; i < kMaskRing; ++i) {
-            mbar_init(&bars.m_full[i], kTma ? kVWarps : kGatherWarps);
+            mbar_init(&bars.m_full[i], kTma ? kKWarps : kGatherWarps);
             mbar_init(&bars.m_empty[i], kSoftWarps * 32);
         }
         mbar_init(&bars.p_full, kSoftWarps * 32);
@@ -180,17 +181,23 @@ __global__ void __launch_bounds__(kThreadsOf<kTma>, 1)
     if (kTma && warp >= kSoftWarps && warp < kMmaWarpOf<kTma>) {
         // ------------------------------------------------------ gather (two engines)
         // Warps 4-7 copy K tiles with tile::gather4 (the tensor-memory-access unit; a warp's
-        // gather4 lanes issue one after another, so four warps share the K rows), warps 8-9
+        // gather4 lanes issue one after another, so four warps share the K rows), warps 8-10
         // copy V tiles with cp.async (the load/store unit), so the two engines work in
-        // parallel.  Each group resolves every row of a tile itself (K warp w: row 32w + t;
-        // V warp w: rows 64w + t and 64w + 32 + t), so the groups only meet at the ring's
-        // barriers.  Groups of 4 rows go to one gather4: an invalid row copies a valid row of
-        // its group (its logits are masked, so it adds nothing), a group with no valid row is
-        // zeroed instead; valid rows of one group share a cache because topk is a multiple of 4.
+        // parallel.  Each group resolves the rows it copies itself, so the groups only meet
+        // at the ring's barriers: K warp w takes row 32w + t (and publishes the tile's
+        // validity word w); V warp w takes the row pairs (2i, 2i + 1) with i = w mod 3, lane t
+        // resolving the t-th and (32 + t)-th row of its list.  Groups of 4 rows go to one
+        // gather4: an invalid row copies a valid row of its group (its logits are masked, so
+        // it adds nothing), a group with no valid row is zeroed instead; valid rows of one
+        // group share a cache because topk is a multiple of 4.
         const int gw = warp - kSoftWarps;
         const bool k_role = gw < kKWarps;
         const int w2 = k_role ? gw : gw - kKWarps;
-        const int R1 = k_role ? 32 * w2 + lane : 64 * w2 + lane, R2 = R1 + 32;  // this thread's rows
+        const int n_pairs = (64 - w2 + kVWarps - 1) / kVWarps;  // V warp: row pairs it copies
+        auto v_row = [&](int q) {  // q-th row of a V warp's list (127 past its end: never copied)
+            return (q >> 1) < n_pairs ? 2 * (w2 + kVWarps * (q >> 1)) + (q & 1) : 127;
+        };
+        const int R1 = k_role ? 32 * w2 + lane : v_row(lane), R2 = k_role ? 0 : v_row(32 + lane);
         int it = 0;
         int64_t g = 0;  // item tiles
         bool ok = true;
@@ -267,6 +274,17 @@ __global__ void __launch_bounds__(kThreadsOf<kTma>, 1)
                 if (k_role) {
                     int c4a[4], graw1;
                     const uint32_t gb1 = group(v1, crd1, raw1, c4a, graw1);
+                    // validity word w of the tile (rows 32w..32w + 31)
+                    const uint32_t bits = __ballot_sync(0xffffffffu, v1);
+                    const int ms = (int)(g % kMaskRing);
+                    if (g >= kMaskRing)
+                        ok = wait_bar(&bars.m_empty[ms], (unsigned)(((g / kMaskRing) - 1) & 1), &s_abort);
+                    ok = __all_sync(0xffffffffu, ok);
+                    if (!ok) break;
+                    if (lane == 0) {
+                        s_mask[ms][w2] = bits;
+                        arrive(&bars.m_full[ms]);
+                    }
                     const int64_t uk = 2 * g;
                     const int sk = (int)(uk % kRing);
                     if (uk >= kRing) ok = wait_bar(&bars.kv_empty[sk], (unsigned)(((uk / kRing) - 1) & 1), &s_abort);
@@ -294,18 +312,8 @@ __global__ void __launch_bounds__(kThreadsOf<kTma>, 1)
                         tma_gather4(dK + kTBlk + R1 * 128, tm, 64, c4a[0], c4a[1], c4a[2], c4a[3], &bars.kv_full[sk]);
                     }
                 } else {
-                    // validity mask of the tile: words 2w and 2w + 1 (rows 64w.., 64w + 32..)
-                    const uint32_t b1 = __ballot_sync(0xffffffffu, v1), b2 = __ballot_sync(0xffffffffu, v2);
-                    const int ms = (int)(g % kMaskRing);
-                    if (g >= kMaskRing)
-                        ok = wait_bar(&bars.m_empty[ms], (unsigned)(((g / kMaskRing) - 1) & 1), &s_abort);
-                    ok = __all_sync(0xffffffffu, ok);
-                    if (!ok) break;
-                    if (lane == 0) {
-                        s_mask[ms][2 * w2] = b1;
-                        s_mask[ms][2 * w2 + 1] = b2;
-                        arrive(&bars.m_full[ms]);
-                    }
+                    (void)v1;
+                    (void)v2;
                     const int64_t uv = 2 * g + 1;
                     const int sv = (int)(uv % kRing);
                     if (uv >= kRing) ok = wait_bar(&bars.kv_empty[sv], (unsigned)(((uv / kRing) - 1) & 1), &s_abort);
@@ -318,10 +326,10 @@ __global__ void __launch_bounds__(kThreadsOf<kTma>, 1)
                     const unsigned long long a2 = reinterpret_cast<unsigned long long>(vp2);
                     const int c = lane & 15;
 #pragma unroll 4
-                    for (int i = 0; i < 32; ++i) {
-                        const int rl = 2 * (i & 15) + (lane >> 4);
-                        const unsigned long long rs = __shfl_sync(0xffffffffu, i < 16 ? a1 : a2, rl);
-                        const int rr = 64 * w2 + (i < 16 ? 0 : 32) + rl;  // row within the tile
+                    for (int k = 0; k < n_pairs; ++k) {
+                        const int q = 2 * k + (lane >> 4);  // position in this warp's row list
+                        const unsigned long long rs = __shfl_sync(0xffffffffu, 2 * k < 32 ? a1 : a2, q & 31);
+                        const int rr = 2 * (w2 + kVWarps * k) + (lane >> 4);  // row within the tile
                         const uint32_t off = (uint32_t)((c >> 3) * kTBlk + rr * 128 + (((c & 7) ^ (rr & 7)) << 4));
                         const __nv_bfloat16 *rp = reinterpret_cast<const __nv_bfloat16 *>(rs);
                         cp_async_16(smem_u32(dV + off), rp ? (const void *)(rp + c * 8) : (const void *)a.vc,
@@ -329,11 +337,13 @@ __global__ void __launch_bounds__(kThreadsOf<kTma>, 1)
                     }
                     cp_async_commit();
                     // the previous tile's V has landed once at most this tile's copies are pending
-                    // (each V thread stands for two of the barrier's 128 arrivals)
+                    // (the barrier counts 128 arrivals: one per thread of V warps 0-1, two per
+                    // thread of V warp 2)
                     if (g > 0) {
                         cp_wait<1>();
                         tc::fence_proxy_async();
-                        arrive2(&bars.kv_full[(uv - 2) % kRing]);
+                        if (w2 == 2) arrive2(&bars.kv_full[(uv - 2) % kRing]);
+                        else arrive(&bars.kv_full[(uv - 2) % kRing]);
                     }
                 }
             }
@@ -355,7 +365,10 @@ __global__ void __launch_bounds__(kThreadsOf<kTma>, 1)
             // publish the last V tile
             cp_wait<0>();
             tc::fence_proxy_async();
-            if (g > 0) arrive2(&bars.kv_full[(2 * (g - 1) + 1) % kRing]);
+            if (g > 0) {
+                if (w2 == 2) arrive2(&bars.kv_full[(2 * (g - 1) + 1) % kRing]);
+                else arrive(&bars.kv_full[(2 * (g - 1) + 1) % kRing]);
+            }
         }
     } else if (!kTma && warp >= kSoftWarps && warp < kMmaWarpOf<kTma>) {
         // ------------------------------------------------------- gather (cp.async)
@@ -474,9 +487,11 @@ __global__ void __launch_bounds__(kThreadsOf<kTma>, 1)
                 ok = ok && wait_bar(&bars.kv_full[slot], (unsigned)((uu / kRing) & 1), &s_abort);
                 return smem_u32(sRing + slot * kTile);
             };
-            auto issue_pv = [&](int64_t gg, int64_t uv, bool first) {
+            // PV of item tile gg (ring use uv); the first of token tok waits until the softmax
+            // has read the previous token's O
+            auto issue_pv = [&](int64_t gg, int64_t uv, bool first, int tok) {
                 ok = ok && wait_bar(&bars.p_full, (unsigned)(gg & 1), &s_abort);
-                if (ok && first && it > 0) ok = wait_bar(&bars.o_free, (unsigned)((it - 1) & 1), &s_abort);
+                if (ok && first && tok > 0) ok = wait_bar(&bars.o_free, (unsigned)((tok - 1) & 1), &s_abort);
                 const uint32_t aV = wait_tile(uv);
                 if (!ok) return;
                 tc::fence_after();
@@ -489,12 +504,16 @@ __global__ void __launch_bounds__(kThreadsOf<kTma>, 1)
                 tc::commit(&bars.o_done);
                 tc::commit(&bars.kv_empty[uv % kRing]);
             };
+            // S(g) goes out before PV(g-1), across token boundaries too, so the softmax finds the
+            // next token's first S ready when it finishes a token
+            int64_t pv_g = -1, pv_u = -1;  // the PV still to issue
+            bool pv_first = false;
+            int pv_tok = 0;
             for (int row = blockIdx.x; row < a.rows && ok; row += gridDim.x, ++it) {
                 ok = wait_bar(&bars.q_full[it & 1], (unsigned)((it >> 1) & 1), &s_abort);
                 if (!ok) break;
                 tc::fence_after();
                 const uint32_t aQ = smem_u32(sQ + (it & 1) * kQBytes);
-                int64_t uv_prev = -1;
                 for (int j = 0; j < nt && ok; ++j, ++g) {
                     const int64_t uk = u, uv = u + 1;
                     u += 2;
@@ -511,11 +530,14 @@ __global__ void __launch_bounds__(kThreadsOf<kTma>, 1)
                     tc::commit(&bars.s_full[g & 1]);
                     tc::commit(&bars.kv_empty[uk % kRing]);
                     if (j == nt - 1) tc::commit(&bars.q_empty[it & 1]);
-                    if (j > 0) issue_pv(g - 1, uv_prev, j == 1);
-                    uv_prev = uv;
+                    if (pv_g >= 0) issue_pv(pv_g, pv_u, pv_first, pv_tok);
+                    pv_g = g;
+                    pv_u = uv;
+                    pv_first = j == 0;
+                    pv_tok = it;
                 }
-                if (ok) issue_pv(g - 1, uv_prev, nt == 1);
             }
+            if (ok && pv_g >= 0) issue_pv(pv_g, pv_u, pv_first, pv_tok);
             if (!ok) s_abort = 1;
             tc::commit(&bars.mma_fin);
             volatile int never = 0;
