@@ -14,16 +14,16 @@
 //              halves of head 16w + l's row): S from TMEM into registers, masked
 //              maximum, exponents, P (bf16) into shared memory for the second MMA,
 //              O rescaled in TMEM only when the maximum grows by > 2^8.
-//   warps 4-7  gather: each thread resolves one item row of tile j (selected entry
-//              of Kc/Vc or window token of the raw cache, zero-filled when
-//              invalid) into a 5-slot ring of 32 KiB 128-byte-swizzled tiles; a
-//              128-bit validity mask per tile goes to a small ring of its own.
-//              Rows are copied either by the tensor-memory-access unit, four rows
-//              per `cp.async.bulk.tensor` `tile::gather4` instruction (one per
-//              64-column half; row coordinates into the cache viewed as a 2-D
-//              tensor, tensor maps one row high), or, where the caches' strides
-//              do not allow that view, by half-warps with 16-byte `cp.async`.
-//              Thread 0 of the group also loads each token's Q by TMA.
+//   gather     resolve each item row of tile j (selected entry of Kc/Vc or window
+//              token of the raw cache; invalid rows are zero) and copy it into a
+//              5-slot ring of 32 KiB 128-byte-swizzled tiles; a 128-bit validity
+//              mask per tile goes to a small ring of its own.  Where the caches can
+//              be viewed as 2-D tensors of rows, warps 4-7 copy K rows by the
+//              tensor-memory-access unit, four rows per `cp.async.bulk.tensor`
+//              `tile::gather4` instruction (one per 64-column half, tensor maps one
+//              row high), and warps 8-10 copy V rows by 16-byte `cp.async`, so the
+//              two engines work in parallel; otherwise warps 4-7 copy both by
+//              `cp.async`.  The first gather thread also loads each token's Q by TMA.
 //   last warp  MMA issuer (one thread): S(g) into one of two TMEM buffers, then
 //              O += P(g-1) V(g-1) (g counted over all the CTA's tokens); completion via
 //              tcgen05.commit.
