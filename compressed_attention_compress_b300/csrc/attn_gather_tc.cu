@@ -600,7 +600,8 @@ __global__ void __launch_bounds__(kThreadsOf<kTma>, 1)
 #pragma unroll
                 for (int q = 0; q < 8; ++q) mx8[q] = -INFINITY;
 #pragma unroll
-                for (int c = 0; c < 64; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], __uint_as_float(v[c]));
+                for (int c = 0; c < 64; c += 2)
+                    mx8[(c >> 1) & 7] = tc::fmax3(mx8[(c >> 1) & 7], __uint_as_float(v[c]), __uint_as_float(v[c + 1]));
                 float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
                                  fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
                 mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16)) * a.scale_log2;

@@ -367,7 +367,9 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                             mx8[c & 7] = fmaxf(mx8[c & 7], visible(hf * 64 + c) ? __uint_as_float(v[c]) : -INFINITY);
                     } else {
 #pragma unroll
-                        for (int c = 0; c < 64; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], __uint_as_float(v[c]));
+                        for (int c = 0; c < 64; c += 2)
+                            mx8[(c >> 1) & 7] =
+                                tc::fmax3(mx8[(c >> 1) & 7], __uint_as_float(v[c]), __uint_as_float(v[c + 1]));
                     }
                 }
                 const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
