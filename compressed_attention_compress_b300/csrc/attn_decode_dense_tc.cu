@@ -18,6 +18,9 @@
 // attn_decode_dense_merge_kernel combines the pieces of every run in list order.
 // The split depends on the whole batch: results are deterministic for a given
 // batch, not bit-identical across batches.
+// The kernel is launched with programmatic stream serialization: its barrier set-up,
+// TMEM allocation and tensor-map prefetch overlap the preceding kernel, and every CTA
+// waits for that kernel's completion (griddepcontrol.wait) before it reads any input.
 //
 // Warp roles:
 //   warp 0      TMA producer (one thread): Q of the run (64 heads x 128), then
@@ -275,15 +278,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     __shared__ int64_t s_p[kMaxB];
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if (threadIdx.x == 0) s_abort = 0;
-    build_sched(a, s_cum, s_E, s_p, blockIdx.x == 0);
-    const Sched sc{s_cum, s_E, s_p, s_cum[a.B]};
-    if (blockIdx.x == 0)
-        for (int b = threadIdx.x; b <= a.B; b += blockDim.x) a.cum[b] = s_cum[b];  // for the merge
-    const int G = gridDim.x;
-    const int u_begin = range_begin(blockIdx.x, sc.total, G), u_end = range_begin(blockIdx.x + 1, sc.total, G);
-    if (u_begin >= u_end) return;  // no tile for this CTA (before any TMEM use)
+    // Launched with programmatic stream serialization: the barriers, the TMEM allocation
+    // and the tensor-map prefetch overlap the preceding kernel (the new block's
+    // compression, typically); every input is read after griddepcontrol.wait.
     if (threadIdx.x == 0) {
+        s_abort = 0;
         mbar_init(&bars.q_full, 1);
         mbar_init(&bars.q_empty, 1);
         for (int i = 0; i < kKRing; ++i) {
@@ -310,9 +309,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (const CUtensorMap *tm : {&tm_q, &tm_kc, &tm_vc, &tm_kr, &tm_vr})
             asm volatile("prefetch.tensormap [%0];\n" ::"l"(tm) : "memory");
     }
+    asm volatile("griddepcontrol.wait;\n" ::: "memory");
+    build_sched(a, s_cum, s_E, s_p, blockIdx.x == 0);  // ends with a block barrier
+    const Sched sc{s_cum, s_E, s_p, s_cum[a.B]};
+    if (blockIdx.x == 0)
+        for (int b = threadIdx.x; b <= a.B; b += blockDim.x) a.cum[b] = s_cum[b];  // for the merge
+    const int G = gridDim.x;
+    const int u_begin = range_begin(blockIdx.x, sc.total, G), u_end = range_begin(blockIdx.x + 1, sc.total, G);
     tc::fence_before();
     __syncthreads();
     tc::fence_after();
+    if (u_begin >= u_end) {  // no tile for this CTA
+        if (warp == 0) tc::tmem_dealloc(s_tmem, 512);
+        return;
+    }
     const uint32_t tmem = s_tmem;
     const uint32_t tS[2] = {tmem, tmem + 128};
     const uint32_t tO[2] = {tmem + 256, tmem + 384};
@@ -816,9 +826,20 @@ cudaError_t launch_attn_decode_dense_tc(const AttnArgs &a, int num_sms, cudaStre
     const int64_t max_tiles = (int64_t)B * g.HG * g.t_max;
     int grid = (int)(max_tiles < num_sms ? max_tiles : num_sms);
     if (grid > kMaxGrid) grid = kMaxGrid;
-    attn_decode_dense_tc_kernel<<<grid, kThreads, kSmemBytes, s>>>(tq, tkc, tvc, tkr, tvr, g);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
+    {
+        cudaLaunchConfig_t mc = {};
+        mc.gridDim = dim3((unsigned)grid);
+        mc.blockDim = dim3(kThreads);
+        mc.dynamicSmemBytes = kSmemBytes;
+        mc.stream = s;
+        cudaLaunchAttribute ma[1];
+        ma[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        ma[0].val.programmaticStreamSerializationAllowed = 1;
+        mc.attrs = ma;
+        mc.numAttrs = 1;
+        e = cudaLaunchKernelEx(&mc, attn_decode_dense_tc_kernel, tq, tkc, tvc, tkr, tvr, g);
+        if (e != cudaSuccess) return e;
+    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(B * g.HG), kH / kMergeWarps);
     cfg.blockDim = dim3(kMergeWarps * 32);

@@ -171,6 +171,9 @@ cudaError_t launch_compress_v4(const CompressArgs &a, const CompressV4Args &v, b
 // entries), instead of one thread walking the m rows one load group at a time.
 template <typename T>
 __global__ void __launch_bounds__(128) compress_staged_kernel(CompressArgs a) {
+    // a kernel launched after this one with programmatic stream serialization may start
+    // its set-up now; it waits for this grid's completion before reading anything
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
     extern __shared__ __align__(16) unsigned char s_raw[];
     float *s_w = reinterpret_cast<float *>(s_raw);
     T *s_x = reinterpret_cast<T *>(s_raw + ((a.m * sizeof(float) + 15) & ~(size_t)15));
