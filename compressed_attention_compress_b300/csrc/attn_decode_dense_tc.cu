@@ -709,7 +709,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32) attn_decode_dense_merge_kern
     // columns 4c..4c+3 of each piece's O, and each piece's maximum and sum (every
     // lane loads them all; they are one 128-byte line per 32 heads).  The running
     // maximum M and the sums are rescaled when a later batch raises M.
-    constexpr int kBatch = 16;
+    constexpr int kBatch = 32;
     float M = -INFINITY, L = 0.f;
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
     for (int i0 = 0; i0 < n; i0 += kBatch) {
