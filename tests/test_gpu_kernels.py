@@ -341,6 +341,41 @@ def test_attn_prefill_parity(lib, dtype, H, d, dense, topk):
     lib.hsa_check()
 
 
+@pytest.mark.parametrize("layout", ["padded_rows", "odd_sequence_stride"])
+def test_attn_prefill_gather_strided(lib, layout):
+    """CSA prefill over cache views: rows padded per sequence keep the tile::gather4
+    copies (row step above E_cap); a sequence stride that is not a whole number of
+    rows takes the cp.async copies.  topk is a multiple of 4 on both."""
+    B, T, H, d, m, W, topk = 2, 40, 64, 128, 4, 128, 64
+    N = 4 * 600
+    E_cap = N // m
+    pos0 = [N - T, 300]
+
+    def view(rows, seed):
+        if layout == "padded_rows":
+            return _randn((B, rows + 3, d), seed).cuda()[:, :rows]
+        flat = _randn((B * (rows * d + 64),), seed).cuda()
+        return flat.as_strided((B, rows, d), (rows * d + 64, d, 1))
+
+    kc, vc, kr, vr = view(E_cap, 131), view(E_cap, 132), view(N, 133), view(N, 134)
+    assert (kc.stride(0) % kc.stride(1) == 0) == (layout == "padded_rows")
+    q = _randn((B, T, H, d), 135)
+    rows_p = (np.asarray(pos0)[:, None] + np.arange(T)[None, :]).reshape(-1)
+    rows_b = np.repeat(np.arange(B), T)
+    idx, cnt = _random_idx([(p + 1) // m for p in rows_p], topk, 136)
+    out = torch.empty((B, T, H, d), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((B, T, H), dtype=torch.float32, device="cuda")
+    lib.hsa_attn_prefill(q.cuda(), kc, vc, m, torch.from_numpy(idx.reshape(B, T, topk)).cuda(),
+                         torch.from_numpy(cnt.reshape(B, T)).cuda(), kr, vr, W, torch.tensor(pos0).cuda(),
+                         scale_of(d), out, lse)
+    torch.cuda.synchronize()
+    ro, rl = oracle.attn_rows(host_np(q.reshape(B * T, H, d)), rows_b, rows_p, host_np(kc), host_np(vc), m, idx,
+                              host_np(kr), host_np(vr), W, scale_of(d))
+    assert_close_out(out.reshape(B * T, H, d), ro, torch.bfloat16)
+    assert_close_lse(lse.reshape(B * T, H), rl)
+    lib.hsa_check()
+
+
 # ---------------------------------------------------------- error paths ---
 
 @pytest.mark.parametrize("H", [16, 64])
