@@ -190,8 +190,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     {
         const int slot = slot0 + tid;
         if (slot < a.topk) {
+            // the slot is inside the [B, topk] index array whatever the count: its load
+            // goes out beside the count's instead of after it
+            const int32_t e_any = a.idx[(int64_t)b * a.topk + slot];
             const int cntb = a.cnt ? min(max(a.cnt[b], 0), a.topk) : a.topk;
-            const int32_t e = slot < cntb ? a.idx[(int64_t)b * a.topk + slot] : -1;
+            const int32_t e = slot < cntb ? e_any : -1;
             if (e >= E) raise_flag(FLAG_ATTN_INDEX);
             if (e >= 0 && e < E) {
                 ksrc = a.kc + (int64_t)b * a.c_sb + (int64_t)e * a.c_se;
