@@ -119,6 +119,21 @@ def cp_decode_step_dense(sh: Shard, q: torch.Tensor, ctx_len: torch.Tensor, *, m
     return ops.lse_merge(allgather(o_r), allgather(lse_r))
 
 
+TC_SLOTS = 2048  # selected entries + window one call of the tensor-core decode kernel takes
+
+
+def split_list(n: int, window: int, slots: int = TC_SLOTS):
+    """Pieces [(c0, c1, window)] of an n-entry list for calls of at most `slots` slots:
+    the window goes with the first piece."""
+    first = max(1, slots - window)
+    out = [(0, min(n, first), window)]
+    c0 = out[0][1]
+    while c0 < n:
+        out.append((c0, min(n, c0 + slots), 0))
+        c0 = out[-1][1]
+    return out
+
+
 class DeviceOps:
     """The per-rank steps on this process's GPU through the library's C ABI
     (workspaces are allocated once here and reused; the library allocates nothing)."""
@@ -126,14 +141,17 @@ class DeviceOps:
     def __init__(self, B: int, H: int, d: int, DI: int, n_local: int, m: int, topk: int, window: int,
                  dtype=torch.bfloat16, device="cuda"):
         """DI = 0: no indexer (the dense step); its attention lists every local entry,
-        so pass topk = n_local."""
+        so pass topk = n_local.  A list longer than one tensor-core call takes is cut
+        into pieces (`split_list`) whose partials are merged here."""
         from . import _lib as L
         self.L = L
         self.topk = topk
+        self.window = window
         self.ws_i = (L.workspace(L.hsa_index_topk_workspace_size(B, 1, DI, n_local, topk), device=device)
                      if DI else None)
-        self.ws_a = L.workspace(L.hsa_attn_decode_workspace_size(dtype, B, H, d, n_local, m, topk, window),
-                                device=device)
+        sizes = [L.hsa_attn_decode_workspace_size(dtype, B, H, d, n_local, m, c1 - c0, w)
+                 for c0, c1, w in split_list(max(topk, 1), window)]
+        self.ws_a = L.workspace(max(sizes), device=device)
 
     def index_topk(self, q_idx, k_idx, E_loc, m, topk):
         B = q_idx.shape[0]
@@ -158,11 +176,20 @@ class DeviceOps:
 
     def attn_partial(self, q, kc, vc, m, loc_idx, k_raw, v_raw, window, ctx_len, scale):
         B, H, d = q.shape
-        out = torch.empty_like(q)
-        lse = torch.empty((B, H), dtype=torch.float32, device=q.device)
-        self.L.hsa_attn_decode(q, kc, vc, m, loc_idx.contiguous(), None, k_raw, v_raw, window, ctx_len, scale,
-                               out, lse, self.ws_a)
-        return out, lse
+        if loc_idx.shape[1] == 0:  # a rank holding no entry: one empty slot, the window alone
+            loc_idx = torch.full((B, 1), -1, dtype=torch.int32, device=q.device)
+        parts = split_list(loc_idx.shape[1], window)
+        outs, lses = [], []
+        for c0, c1, w in parts:
+            out = torch.empty_like(q)
+            lse = torch.empty((B, H), dtype=torch.float32, device=q.device)
+            self.L.hsa_attn_decode(q, kc, vc, m, loc_idx[:, c0:c1].contiguous(), None, k_raw, v_raw, w, ctx_len,
+                                   scale, out, lse, self.ws_a)
+            outs.append(out)
+            lses.append(lse)
+        if len(parts) == 1:
+            return outs[0], lses[0]
+        return self.lse_merge(torch.stack(outs), torch.stack(lses))
 
     def lse_merge(self, parts_o, parts_lse):
         out = torch.empty(parts_o.shape[1:], dtype=parts_o.dtype, device=parts_o.device)

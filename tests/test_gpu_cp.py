@@ -143,14 +143,14 @@ def test_cp_decode_step_device(L, world):
     L.hsa_check()
 
 
-@pytest.mark.parametrize("world", [1, 2, 4])
-def test_cp_decode_step_dense_device(L, world):
+@pytest.mark.parametrize("world,E_cap", [(1, 2048), (2, 2048), (4, 2048), (5, 2048), (4, 3)])
+def test_cp_decode_step_dense_device(L, world, E_cap):
     """HCA shape (m = 128, 128-token window) on a 256k-token context: each rank's
     attention over all its visible entries, merged, matches the oracle of the
-    unsharded dense step (one rank's list exceeds the tensor-core kernel's 2,048
-    slots at world 1, so the general kernel is covered too)."""
+    unsharded dense step (at world 1 a rank's 2,048 entries plus the window exceed
+    one tensor-core call, so its list goes in two pieces merged on the rank; with 3
+    entries over 4 ranks one rank holds none and attends to the window alone)."""
     B, H, d, m, W = 2, 64, 128, 128, 128
-    E_cap = 2048
     N = E_cap * m
     dev = torch.device("cuda")
     g = torch.Generator().manual_seed(60 + world)
@@ -166,7 +166,7 @@ def test_cp_decode_step_dense_device(L, world):
         e0, e1 = cp.shard_bounds(E_cap, world, r)
         sh = cp.Shard(rank=r, world=world, e0=e0, kc=kc[:, e0:e1].contiguous().to(dev),
                       vc=vc[:, e0:e1].contiguous().to(dev), k_idx=torch.empty(0, dtype=torch.int8, device=dev),
-                      k_raw=k_raw.to(dev), v_raw=v_raw.to(dev), window_rank=0)
+                      k_raw=k_raw.to(dev), v_raw=v_raw.to(dev), window_rank=world - 1)
         ops = cp.DeviceOps(B, H, d, 0, e1 - e0, m, e1 - e0, W)
         out, lse = cp.cp_decode_step_dense(sh, q.to(dev), ctx.to(dev), m=m, window=W, scale=scale,
                                            allgather=ag, ops=ops)
