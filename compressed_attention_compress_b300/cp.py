@@ -24,6 +24,9 @@ Dense (HCA) layers (QbitAI article, the HCA paragraph: dense attention over ever
 compressed entry) shard the same way with steps 1-2 left out: every rank attends to
 all of its visible entries, the window rank adds the window, and the partials are
 merged (`cp_decode_step_dense`).
+A prefill chunk can instead shard its query rows with the cache replicated
+(`cp_prefill_rows`): every row's selection and attention use only that row's data,
+so ranks need no exchange besides gathering the outputs.
 """
 from __future__ import annotations
 
@@ -119,6 +122,47 @@ def cp_decode_step_dense(sh: Shard, q: torch.Tensor, ctx_len: torch.Tensor, *, m
     return ops.lse_merge(allgather(o_r), allgather(lse_r))
 
 
+def row_bounds(T: int, world: int, rank: int) -> tuple[int, int]:
+    """Contiguous, nearly equal query-row ranges of a T-token chunk: rank r takes [t0, t1)."""
+    per = (T + world - 1) // world
+    t0 = min(T, rank * per)
+    return t0, min(T, t0 + per)
+
+
+def cp_prefill_rows(rank: int, world: int, q: torch.Tensor, q_idx, k_idx, kc, vc, k_raw, v_raw,
+                    q_pos0: torch.Tensor, *, m: int, topk: int, window: int, scale: float, ops,
+                    allgather: Callable[[torch.Tensor], torch.Tensor] | None = None):
+    """Chunked prefill with the chunk's query rows sharded over ranks and the cache
+    replicated (no exchange): rank r selects (CSA: q_idx and k_idx given; HCA: None)
+    and attends for the tokens [t0, t1) of its row range, whose positions start at
+    q_pos0 + t0.  q [B, T, H, d], q_idx [B, T, DI].  Returns (t0, out [B, t1 - t0, H, d],
+    lse, idx or None); with `allgather`, out and lse of the whole chunk instead (every
+    rank's range padded to the longest)."""
+    B, T = q.shape[:2]
+    t0, t1 = row_bounds(T, world, rank)
+    pos = (q_pos0 + t0).contiguous()
+    idx = cnt = None
+    if t1 > t0:
+        if q_idx is not None:
+            idx, cnt = ops.index_topk_rows(q_idx[:, t0:t1].contiguous(), k_idx, pos, m, topk)
+        out, lse = ops.attn_prefill(q[:, t0:t1].contiguous(), kc, vc, m, idx, cnt, k_raw, v_raw, window, pos,
+                                    scale)
+    else:  # more ranks than rows: nothing here
+        out = torch.empty((B, 0) + tuple(q.shape[2:]), dtype=q.dtype, device=q.device)
+        lse = torch.empty((B, 0, q.shape[2]), dtype=torch.float32, device=q.device)
+    if allgather is None:
+        return t0, out, lse, idx
+    per = (T + world - 1) // world
+    pad_o = torch.zeros((B, per) + tuple(out.shape[2:]), dtype=out.dtype, device=out.device)
+    pad_l = torch.zeros((B, per) + tuple(lse.shape[2:]), dtype=lse.dtype, device=lse.device)
+    pad_o[:, :t1 - t0] = out
+    pad_l[:, :t1 - t0] = lse
+    go, gl = allgather(pad_o), allgather(pad_l)  # [world, B, per, ...]
+    full_o = torch.cat([go[r, :, :row_bounds(T, world, r)[1] - row_bounds(T, world, r)[0]] for r in range(world)], 1)
+    full_l = torch.cat([gl[r, :, :row_bounds(T, world, r)[1] - row_bounds(T, world, r)[0]] for r in range(world)], 1)
+    return 0, full_o, full_l, idx
+
+
 TC_SLOTS = 2048  # selected entries + window one call of the tensor-core decode kernel takes
 
 
@@ -190,6 +234,26 @@ class DeviceOps:
         if len(parts) == 1:
             return outs[0], lses[0]
         return self.lse_merge(torch.stack(outs), torch.stack(lses))
+
+    def index_topk_rows(self, q_idx, k_idx, q_pos0, m, topk):
+        """Top-k of several query rows per sequence (prefill rows): idx [B, T, topk], cnt [B, T]."""
+        B, T, DI = q_idx.shape
+        idx = torch.empty((B, T, topk), dtype=torch.int32, device=q_idx.device)
+        cnt = torch.empty((B, T), dtype=torch.int32, device=q_idx.device)
+        ws = self.L.workspace(self.L.hsa_index_topk_workspace_size(B, T, DI, k_idx.shape[1], topk),
+                              device=q_idx.device)
+        self.L.hsa_index_topk(q_idx, k_idx, q_pos0, m, topk, idx, cnt, ws)
+        return idx, cnt
+
+    def attn_prefill(self, q, kc, vc, m, idx, cnt, k_raw, v_raw, window, q_pos0, scale):
+        B, T, H, d = q.shape
+        out = torch.empty_like(q)
+        lse = torch.empty((B, T, H), dtype=torch.float32, device=q.device)
+        topk = idx.shape[-1] if idx is not None else 0
+        ws = self.L.workspace(self.L.hsa_attn_prefill_workspace_size(q.dtype, B, T, H, d, kc.shape[1], m, topk,
+                                                                     window), device=q.device)
+        self.L.hsa_attn_prefill(q, kc, vc, m, idx, cnt, k_raw, v_raw, window, q_pos0, scale, out, lse, ws)
+        return out, lse
 
     def lse_merge(self, parts_o, parts_lse):
         out = torch.empty(parts_o.shape[1:], dtype=parts_o.dtype, device=parts_o.device)

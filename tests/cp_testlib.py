@@ -148,3 +148,33 @@ def full_reference_dense(x, ctx_len, m, window, scale):
     o, l = oracle.attn_rows(x["q"], np.arange(B), p, x["kc"], x["vc"], m, None, x["k_raw"], x["v_raw"], window,
                             scale)
     return o, l
+
+
+class PrefillOracleOps:
+    """Per-rank prefill steps (replicated cache) computed by the oracle."""
+
+    def index_topk_rows(self, q_idx, k_idx, q_pos0, m, topk):
+        B, T, DI = q_idx.shape
+        rows_b = np.repeat(np.arange(B), T)
+        rows_p = (q_pos0.numpy()[:, None] + np.arange(T)[None, :]).reshape(-1)
+        idx, cnt = oracle.index_topk_rows(q_idx.numpy().reshape(B * T, DI), rows_b, rows_p, k_idx.numpy(), m, topk)
+        return torch.from_numpy(idx.reshape(B, T, topk)), torch.from_numpy(cnt.reshape(B, T))
+
+    def attn_prefill(self, q, kc, vc, m, idx, cnt, k_raw, v_raw, window, q_pos0, scale):
+        B, T, H, d = q.shape
+        rows_b = np.repeat(np.arange(B), T)
+        rows_p = (q_pos0.numpy()[:, None] + np.arange(T)[None, :]).reshape(-1)
+        ia = None if idx is None else idx.numpy().reshape(B * T, -1)
+        o, l = oracle.attn_rows(q.numpy().reshape(B * T, H, d), rows_b, rows_p, kc.numpy(), vc.numpy(), m, ia,
+                                k_raw.numpy(), v_raw.numpy(), window, scale)
+        return torch.from_numpy(o.reshape(B, T, H, d)), torch.from_numpy(l.reshape(B, T, H))
+
+
+def prefill_case(seed: int, B: int, T: int, E_cap: int, m: int, H: int, d: int, DI: int):
+    """Seeded chunk inputs: q [B, T, H, d] fp64, q_idx [B, T, DI] int8, and a replicated cache."""
+    g = np.random.default_rng(seed)
+    N = E_cap * m
+    return dict(q=g.standard_normal((B, T, H, d)), q_idx=g.integers(-127, 128, (B, T, DI)).astype(np.int8),
+                kc=g.standard_normal((B, E_cap, d)), vc=g.standard_normal((B, E_cap, d)),
+                k_raw=g.standard_normal((B, N, d)), v_raw=g.standard_normal((B, N, d)),
+                k_idx=g.integers(-127, 128, (B, E_cap, DI)).astype(np.int8))

@@ -13,7 +13,8 @@ import torch.multiprocessing as mp
 
 import oracle
 from compressed_attention_compress_b300 import cp
-from tests.cp_testlib import OracleOps, ThreadGroup, cp_case, full_reference, full_reference_dense
+from tests.cp_testlib import (OracleOps, PrefillOracleOps, ThreadGroup, cp_case, full_reference,
+                              full_reference_dense, prefill_case)
 
 M, H, D, DI, TOPK, W = 4, 4, 16, 32, 8, 8
 M_HCA = 16          # HCA-layer block size of the dense cases (the window W < M_HCA)
@@ -73,13 +74,49 @@ DENSE_CASES = [
 ]
 
 
-def _gloo_worker(rank, world, port, case, dense=False):
+PREFILL_CASES = [
+    # (seed, B, T, E_cap, q_pos0 per sequence, csa)
+    (31, 2, 13, 40, [147, 20], True),     # CSA: index and attention per row; sequence 1 starts with few entries
+    (32, 1, 5, 40, [100], False),         # HCA; 5 rows over up to 4 ranks
+    (33, 1, 2, 40, [60], True),           # fewer rows than ranks: some ranks have none
+]
+
+
+def _prefill_run(rank, world, x, pos0, csa, allgather):
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a))
+    return cp.cp_prefill_rows(rank, world, t(x["q"]), t(x["q_idx"]) if csa else None, t(x["k_idx"]) if csa else None,
+                              t(x["kc"]), t(x["vc"]), t(x["k_raw"]), t(x["v_raw"]),
+                              torch.tensor(pos0, dtype=torch.int64), m=M, topk=TOPK, window=W, scale=SCALE,
+                              ops=PrefillOracleOps(), allgather=allgather)
+
+
+def _prefill_check(res, x, pos0, csa):
+    ops = PrefillOracleOps()
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a))
+    pos = torch.tensor(pos0, dtype=torch.int64)
+    idx = cnt = None
+    if csa:
+        idx, cnt = ops.index_topk_rows(t(x["q_idx"]), t(x["k_idx"]), pos, M, TOPK)
+    ro, rl = ops.attn_prefill(t(x["q"]), t(x["kc"]), t(x["vc"]), M, idx, cnt, t(x["k_raw"]), t(x["v_raw"]), W, pos,
+                              SCALE)
+    for t0, out, lse, _ in res:
+        assert t0 == 0
+        np.testing.assert_array_equal(out.numpy(), ro.numpy())
+        np.testing.assert_array_equal(lse.numpy(), rl.numpy())
+
+
+def _gloo_worker(rank, world, port, case, dense=False, prefill=False):
     os.environ["MASTER_ADDR"] = "127.0.0.1"
     os.environ["MASTER_PORT"] = str(port)
     import torch.distributed as dist
     dist.init_process_group("gloo", rank=rank, world_size=world)
     try:
         oracle.build()
+        if prefill:
+            seed, B, T, E_cap, pos0, csa = case
+            x = prefill_case(seed, B, T, E_cap, M, H, D, DI)
+            _prefill_check([_prefill_run(rank, world, x, pos0, csa, cp.torch_allgather())], x, pos0, csa)
+            return
         if dense:
             seed, B, E_cap, ctx = case
             x = cp_case(seed, B, E_cap, M_HCA, H, D, DI)
@@ -132,6 +169,24 @@ def test_cp_dense_thread_ranks(case, world):
     tg = ThreadGroup(world)
     res = tg.run(lambda r, ag: _run_rank_dense(r, world, x, E_cap, ctx, ag, window_rank=world // 2))
     _check_dense(res, x, ctx)
+
+
+@pytest.mark.parametrize("case", PREFILL_CASES, ids=["csa", "hca", "few_rows"])
+def test_cp_prefill_rows_gloo_two_ranks(case):
+    oracle.build()
+    mp.spawn(_gloo_worker, args=(2, _free_port(), case, False, True), nprocs=2, join=True)
+
+
+@pytest.mark.parametrize("world", [1, 3, 4])
+@pytest.mark.parametrize("case", PREFILL_CASES, ids=["csa", "hca", "few_rows"])
+def test_cp_prefill_rows_thread_ranks(case, world):
+    """Rows sharded, cache replicated: the gathered outputs equal the unsharded oracle
+    bit for bit (each row's selection and attention use only that row's data)."""
+    oracle.build()
+    seed, B, T, E_cap, pos0, csa = case
+    x = prefill_case(seed, B, T, E_cap, M, H, D, DI)
+    tg = ThreadGroup(world)
+    _prefill_check(tg.run(lambda r, ag: _prefill_run(r, world, x, pos0, csa, ag)), x, pos0, csa)
 
 
 def test_cp_union_of_local_topk_is_global_topk():

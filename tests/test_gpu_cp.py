@@ -180,3 +180,41 @@ def test_cp_decode_step_dense_device(L, world, E_cap):
         assert_close_out(out, ro, torch.bfloat16)
         assert_close_lse(lse, rl)
     L.hsa_check()
+
+
+@pytest.mark.parametrize("world", [2, 3])
+@pytest.mark.parametrize("csa", [True, False], ids=["csa", "hca"])
+def test_cp_prefill_rows_device(L, world, csa):
+    """Prefill rows sharded over ranks, cache replicated: each rank's selection is the
+    single call's for its rows, bit for bit, and the gathered outputs match it."""
+    B, T, H, d, W, DI, topk = 1, 48, 64, 128, 128, 64, 512
+    m, E_cap = (4, 8192) if csa else (128, 256)
+    N = E_cap * m
+    dev = torch.device("cuda")
+    g = torch.Generator().manual_seed(70 + world + 10 * csa)
+    kc = torch.randn((B, E_cap, d), generator=g).to(torch.bfloat16).to(dev)
+    vc = torch.randn((B, E_cap, d), generator=g).to(torch.bfloat16).to(dev)
+    k_raw = torch.randn((B, N, d), generator=g).to(torch.bfloat16).to(dev)
+    v_raw = torch.randn((B, N, d), generator=g).to(torch.bfloat16).to(dev)
+    q = torch.randn((B, T, H, d), generator=g).to(torch.bfloat16).to(dev)
+    k_idx = torch.randint(-127, 128, (B, E_cap, DI), generator=g, dtype=torch.int16).to(torch.int8).to(dev)
+    q_idx = torch.randint(-127, 128, (B, T, DI), generator=g, dtype=torch.int16).to(torch.int8).to(dev)
+    pos0 = torch.tensor([N - T], dtype=torch.int64, device=dev)
+    scale = 1.0 / d ** 0.5
+    ops = cp.DeviceOps(B, H, d, DI if csa else 0, E_cap, m, topk, W)
+    args = (q, q_idx if csa else None, k_idx if csa else None, kc, vc, k_raw, v_raw, pos0)
+    kw = dict(m=m, topk=topk, window=W, scale=scale, ops=ops)
+    _, ref_o, ref_l, ref_idx = cp.cp_prefill_rows(0, 1, *args, **kw)
+
+    def rank_fn(r, ag):
+        res = cp.cp_prefill_rows(r, world, *args, **kw, allgather=ag)
+        t0, t1 = cp.row_bounds(T, world, r)
+        torch.cuda.synchronize()
+        return res, t0, t1
+
+    for (_, out, lse, idx), t0, t1 in ThreadGroup(world).run(rank_fn):
+        if csa:
+            assert torch.equal(idx, ref_idx[:, t0:t1])
+        assert_close_out(out.reshape(B * T, H, d), ref_o.reshape(B * T, H, d).float().cpu().numpy(), torch.bfloat16)
+        assert_close_lse(lse.reshape(B * T, H), ref_l.reshape(B * T, H).cpu().numpy())
+    L.hsa_check()
