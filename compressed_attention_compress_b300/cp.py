@@ -1,5 +1,6 @@
-"""Context-parallel CSA decode over one long sequence whose compressed entries are
-sharded across ranks.
+"""Context parallelism for this attention path: decode over one long sequence whose
+compressed entries are sharded across ranks (CSA and HCA layers), and chunked
+prefill with the query rows sharded.
 
 Rank r of `world` holds a contiguous range [e0, e0 + n_local) of every sequence's
 compressed entries (Kc, Vc and the indexer keys kI); the rank `window_rank` also
@@ -136,8 +137,8 @@ def cp_prefill_rows(rank: int, world: int, q: torch.Tensor, q_idx, k_idx, kc, vc
     replicated (no exchange): rank r selects (CSA: q_idx and k_idx given; HCA: None)
     and attends for the tokens [t0, t1) of its row range, whose positions start at
     q_pos0 + t0.  q [B, T, H, d], q_idx [B, T, DI].  Returns (t0, out [B, t1 - t0, H, d],
-    lse, idx or None); with `allgather`, out and lse of the whole chunk instead (every
-    rank's range padded to the longest)."""
+    lse, this rank's idx or None); with `allgather`, (0, out, lse) of the whole chunk
+    (every rank's range padded to the longest for the gather) and this rank's idx."""
     B, T = q.shape[:2]
     t0, t1 = row_bounds(T, world, rank)
     pos = (q_pos0 + t0).contiguous()
@@ -158,8 +159,9 @@ def cp_prefill_rows(rank: int, world: int, q: torch.Tensor, q_idx, k_idx, kc, vc
     pad_o[:, :t1 - t0] = out
     pad_l[:, :t1 - t0] = lse
     go, gl = allgather(pad_o), allgather(pad_l)  # [world, B, per, ...]
-    full_o = torch.cat([go[r, :, :row_bounds(T, world, r)[1] - row_bounds(T, world, r)[0]] for r in range(world)], 1)
-    full_l = torch.cat([gl[r, :, :row_bounds(T, world, r)[1] - row_bounds(T, world, r)[0]] for r in range(world)], 1)
+    lens = [row_bounds(T, world, r)[1] - row_bounds(T, world, r)[0] for r in range(world)]
+    full_o = torch.cat([go[r, :, :lens[r]] for r in range(world)], 1)
+    full_l = torch.cat([gl[r, :, :lens[r]] for r in range(world)], 1)
     return 0, full_o, full_l, idx
 
 
