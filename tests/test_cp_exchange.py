@@ -203,3 +203,22 @@ def test_cp_union_of_local_topk_is_global_topk():
         for a, b in zip(bounds[:-1], bounds[1:]):
             union += order(range(a, b))[:k]
         assert sorted(order(union)[:k]) == sorted(order(range(n))[:k])
+
+
+def test_split_list_and_row_bounds():
+    """Host helpers: the pieces of a per-rank list cover it once, in order, each call at
+    most TC_SLOTS slots with the window on the first piece only; row ranges cover a
+    chunk once, nearly equal, in rank order."""
+    for n in [1, 2, 100, 1919, 1920, 1921, 2048, 4096, 5000]:
+        for w in [0, 1, 128, 2047]:
+            ps = cp.split_list(n, w)
+            assert ps[0][0] == 0 and ps[-1][1] == n
+            assert all(a[1] == b[0] for a, b in zip(ps, ps[1:]))
+            assert ps[0][2] == w and all(p[2] == 0 for p in ps[1:])
+            assert all(c1 > c0 and c1 - c0 + ww <= cp.TC_SLOTS for c0, c1, ww in ps)
+    for T in [1, 5, 13, 48, 8192]:
+        for world in [1, 2, 3, 4, 7]:
+            rb = [cp.row_bounds(T, world, r) for r in range(world)]
+            assert rb[0][0] == 0 and rb[-1][1] == T
+            assert all(a[1] == b[0] for a, b in zip(rb, rb[1:]))
+            assert max(t1 - t0 for t0, t1 in rb) <= -(-T // world)
