@@ -185,7 +185,7 @@ __global__ void __launch_bounds__(kThreadsOf<kTma>, 1)
         // copy V tiles with cp.async (the load/store unit), so the two engines work in
         // parallel.  Each group resolves the rows it copies itself, so the groups only meet
         // at the ring's barriers: K warp w takes row 32w + t (and publishes the tile's
-        // validity word w); V warp w takes the row pairs (2i, 2i + 1) with i = w mod 3, lane t
+        // validity word w); V warp w takes the row pairs (2i, 2i + 1) with i ≡ w (mod 3), lane t
         // resolving the t-th and (32 + t)-th row of its list.  Groups of 4 rows go to one
         // gather4: an invalid row copies a valid row of its group (its logits are masked, so
         // it adds nothing), a group with no valid row is zeroed instead; valid rows of one
